@@ -1,0 +1,94 @@
+// Internal declarations shared by the host glue and the kernels of libqwm.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "qwm.h"
+
+namespace qwm {
+
+constexpr int kTile = 128;   // token slots per cache tile
+constexpr int kGroup = 32;   // channels per quantisation group
+
+struct SegmentRec {
+  int64_t first_tile;
+  int64_t n_tiles;
+  int64_t n_tokens;
+  int32_t version;
+};
+
+}  // namespace qwm
+
+struct qwm_ctx {
+  qwm_config cfg;
+  qwm_layout lay;
+  int device;
+  int G;          // groups per head
+  int ib;         // index bytes per slot
+  int esz;        // element size of the configured dtype
+  uint8_t* cache;
+  uint8_t* state;
+  uint8_t* ws;
+  // typed views into the state buffer
+  uint32_t* status;
+  float* s;
+  float* w;
+  float* lambda;
+  float* energy;
+  void* centroids;
+  float* basis;     // [max_versions][H][r][d]
+  int2* tiles;      // [max_tiles] (version, valid)
+  int32_t* iters;   // [H] eigen-solver iterations of the last calibrate
+  // host bookkeeping
+  int64_t n_tokens;
+  int64_t n_tiles;
+  int32_t version;       // -1 before the first calibration
+  bool centroids_set;
+  int32_t attend_kernel;
+  std::vector<qwm::SegmentRec> segs;
+};
+
+namespace qwm {
+
+// ---- launchers (each returns cudaGetLastError() of its launch) ----
+cudaError_t launch_append(const qwm_ctx* c, const void* k, const void* v, int64_t n,
+                          int64_t tile0, int32_t version, cudaStream_t st);
+cudaError_t launch_gram(const qwm_ctx* c, const void* q, int64_t n_h, cudaStream_t st);
+cudaError_t launch_eig(const qwm_ctx* c, int64_t n_h, int32_t version, cudaStream_t st);
+cudaError_t launch_group_weights(const qwm_ctx* c, cudaStream_t st);
+cudaError_t launch_attend_simt(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                               cudaStream_t st);
+cudaError_t launch_attend_mma(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                              cudaStream_t st);
+bool attend_mma_supported(const qwm_ctx* c);
+size_t gram_workspace_bytes(const qwm_config& cfg);
+
+// ---- device helpers ----
+__device__ __forceinline__ float load_elem(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float load_elem(const __nv_bfloat16* p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+
+// Tile section offsets (bytes) for one configuration.
+struct TileOffsets {
+  int idx, kcode, kqp, e, vcode, vqp, bytes;
+};
+
+inline TileOffsets tile_offsets(const qwm_layout& L) {
+  TileOffsets t;
+  t.idx = (int)L.off_idx;
+  t.kcode = (int)L.off_kcode;
+  t.kqp = (int)L.off_kqp;
+  t.e = (int)L.off_e;
+  t.vcode = (int)L.off_vcode;
+  t.vqp = (int)L.off_vqp;
+  t.bytes = (int)L.tile_bytes;
+  return t;
+}
+
+}  // namespace qwm

@@ -1,0 +1,266 @@
+"""Thin Python binding of libqwm (ctypes).
+
+Argument marshalling only: every step of calibrate / append / attend runs in
+the CUDA library.  PyTorch provides device memory and the current stream.
+There is no fallback: if libqwm.so is missing or fails to load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqwm.so")
+
+QWM_F32, QWM_BF16 = 0, 1
+DEV_NOT_CONVERGED, DEV_SATURATED = 0x1, 0x2
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA, KERNEL_TC = 0, 1, 2, 3
+
+STATUS = {0: "QWM_OK", 1: "QWM_ERR_INVALID_ARG", 2: "QWM_ERR_UNSUPPORTED", 3: "QWM_ERR_CAPACITY",
+          4: "QWM_ERR_NOT_CALIBRATED", 5: "QWM_ERR_NOT_CONVERGED", 6: "QWM_ERR_CUDA",
+          7: "QWM_ERR_OOM", 8: "QWM_ERR_DEVICE"}
+
+
+class qwm_config(ctypes.Structure):
+    _fields_ = [("heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("rank", ctypes.c_int32), ("n_centroids", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("max_tokens", ctypes.c_int64), ("max_versions", ctypes.c_int32),
+                ("max_iter", ctypes.c_int32), ("oversample", ctypes.c_int32),
+                ("max_hist", ctypes.c_int32)]
+
+
+class qwm_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("cache_bytes", "state_bytes", "workspace_bytes",
+                                                "tile_bytes", "bytes_per_token")] + \
+               [("max_tiles", ctypes.c_int64)] + \
+               [(n, ctypes.c_size_t) for n in ("off_idx", "off_kcode", "off_kqp", "off_e", "off_vcode",
+                                                "off_vqp", "st_status", "st_s", "st_w", "st_lambda",
+                                                "st_energy", "st_centroids", "st_basis", "st_tiles",
+                                                "st_iters")]
+
+
+class QwmError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+EXPORTS = ["qwm_status_string", "qwm_sizes", "qwm_create", "qwm_destroy", "qwm_set_centroids",
+           "qwm_calibrate", "qwm_set_calibration", "qwm_get_calibration", "qwm_append",
+           "qwm_attend", "qwm_rewind", "qwm_get_status", "qwm_peek_status_bits",
+           "qwm_set_attend_kernel", "qwm_resolved_attend_kernel", "qwm_num_tokens", "qwm_num_tiles", "qwm_num_segments",
+           "qwm_version"]
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libqwm.so (built in-tree by build.py); raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libqwm.so not found at {LIB_PATH}: run bit_kv_cache_qwm_gb300/build.py")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, F, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+    L.qwm_status_string.restype = ctypes.c_char_p
+    L.qwm_status_string.argtypes = [ctypes.c_int]
+    sig = {
+        "qwm_sizes": [P(qwm_config), P(qwm_layout)],
+        "qwm_create": [P(qwm_config), VP, VP, VP, P(VP)],
+        "qwm_destroy": [VP],
+        "qwm_set_centroids": [VP, VP, VP],
+        "qwm_calibrate": [VP, VP, I64, VP],
+        "qwm_set_calibration": [VP, P(F), P(F), VP],
+        "qwm_get_calibration": [VP, P(F), P(F), P(F), P(F), VP],
+        "qwm_append": [VP, VP, VP, I64, VP],
+        "qwm_attend": [VP, VP, I64, F, VP, VP],
+        "qwm_rewind": [VP, I32],
+        "qwm_get_status": [VP, VP],
+        "qwm_peek_status_bits": [VP, P(ctypes.c_uint32), VP],
+        "qwm_set_attend_kernel": [VP, I32],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    for name, rt in [("qwm_resolved_attend_kernel", I32), ("qwm_num_tokens", I64), ("qwm_num_tiles", I64), ("qwm_num_segments", I32),
+                     ("qwm_version", I32)]:
+        fn = getattr(L, name)
+        fn.argtypes = [VP]
+        fn.restype = rt
+    _lib = L
+    return L
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise QwmError(st, what)
+
+
+def _stream() -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _fptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def make_config(heads, head_dim, rank, n_centroids, dtype="bf16", max_tokens=4096, max_versions=4,
+                max_iter=64, oversample=16, max_hist=4096) -> qwm_config:
+    return qwm_config(heads=heads, head_dim=head_dim, group=32, rank=rank, n_centroids=n_centroids,
+                      dtype=QWM_BF16 if dtype == "bf16" else QWM_F32, max_tokens=max_tokens,
+                      max_versions=max_versions, max_iter=max_iter, oversample=oversample,
+                      max_hist=max_hist)
+
+
+def qwm_sizes(cfg: qwm_config) -> qwm_layout:
+    out = qwm_layout()
+    _check(lib().qwm_sizes(ctypes.byref(cfg), ctypes.byref(out)), "qwm_sizes")
+    return out
+
+
+class Qwm:
+    """One libqwm context with its device buffers allocated through torch."""
+
+    def __init__(self, heads, head_dim, rank, n_centroids, dtype="bf16", max_tokens=4096,
+                 max_versions=4, max_iter=64, oversample=16, max_hist=4096, device=None):
+        self.cfg = make_config(heads, head_dim, rank, n_centroids, dtype, max_tokens, max_versions,
+                               max_iter, oversample, max_hist)
+        self.layout = qwm_sizes(self.cfg)
+        self.dtype = dtype
+        self.tdtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.device = (torch.device(device) if device is not None
+                       else torch.device("cuda", torch.cuda.current_device()))
+        L = self.layout
+        with torch.cuda.device(self.device):
+            self.cache = torch.empty(max(L.cache_bytes, 256), dtype=torch.uint8, device=self.device)
+            self.state = torch.empty(max(L.state_bytes, 256), dtype=torch.uint8, device=self.device)
+            self.workspace = torch.empty(max(L.workspace_bytes, 256), dtype=torch.uint8, device=self.device)
+            torch.cuda.synchronize(self.device)
+            h = ctypes.c_void_p()
+            _check(lib().qwm_create(ctypes.byref(self.cfg), ctypes.c_void_p(self.cache.data_ptr()),
+                                    ctypes.c_void_p(self.state.data_ptr()),
+                                    ctypes.c_void_p(self.workspace.data_ptr()), ctypes.byref(h)),
+                   "qwm_create")
+        self._h = h
+
+    # ---- helpers
+    def _t(self, x: torch.Tensor, shape, what):
+        if not isinstance(x, torch.Tensor) or x.device != self.device or x.dtype != self.tdtype:
+            raise ValueError(f"{what}: expected a {self.tdtype} tensor on {self.device}")
+        if tuple(x.shape) != tuple(shape) or not x.is_contiguous():
+            raise ValueError(f"{what}: expected contiguous shape {tuple(shape)}, got {tuple(x.shape)}")
+        return ctypes.c_void_p(x.data_ptr())
+
+    @property
+    def handle(self):
+        return self._h
+
+    # ---- the calls
+    def set_centroids(self, cent: torch.Tensor):
+        c = self.cfg
+        _check(lib().qwm_set_centroids(self._h, self._t(cent, (c.heads, c.n_centroids, c.head_dim), "centroids"),
+                                       _stream()), "qwm_set_centroids")
+
+    def calibrate(self, q_hist: torch.Tensor):
+        c = self.cfg
+        n_h = q_hist.shape[1]
+        _check(lib().qwm_calibrate(self._h, self._t(q_hist, (c.heads, n_h, c.head_dim), "q_hist"), n_h,
+                                   _stream()), "qwm_calibrate")
+
+    def set_calibration(self, s, U):
+        c = self.cfg
+        s = np.ascontiguousarray(np.asarray(s, dtype=np.float32).reshape(c.heads, c.head_dim))
+        U = np.ascontiguousarray(np.asarray(U, dtype=np.float32).reshape(c.heads, c.rank, c.head_dim))
+        _check(lib().qwm_set_calibration(self._h, _fptr(s), _fptr(U) if c.rank else None, _stream()),
+               "qwm_set_calibration")
+
+    def get_calibration(self) -> dict:
+        c = self.cfg
+        s = np.zeros((c.heads, c.head_dim), np.float32)
+        U = np.zeros((c.heads, c.rank, c.head_dim), np.float32)
+        lam = np.zeros((c.heads, c.rank), np.float32)
+        en = np.zeros(c.heads, np.float32)
+        _check(lib().qwm_get_calibration(self._h, _fptr(s), _fptr(U) if c.rank else None,
+                                         _fptr(lam) if c.rank else None, _fptr(en), _stream()),
+               "qwm_get_calibration")
+        return {"s": s, "U": U, "lambda": lam, "energy": en}
+
+    def append(self, k: torch.Tensor, v: torch.Tensor):
+        c = self.cfg
+        n = k.shape[1]
+        shape = (c.heads, n, c.head_dim)
+        _check(lib().qwm_append(self._h, self._t(k, shape, "k"), self._t(v, shape, "v"), n, _stream()),
+               "qwm_append")
+
+    def attend(self, q: torch.Tensor, out: Optional[torch.Tensor] = None, scale: float = 0.0) -> torch.Tensor:
+        c = self.cfg
+        M = q.shape[1]
+        if out is None:
+            out = torch.empty_like(q)
+        _check(lib().qwm_attend(self._h, self._t(q, (c.heads, M, c.head_dim), "q"), M, float(scale),
+                                self._t(out, (c.heads, M, c.head_dim), "out"), _stream()), "qwm_attend")
+        return out
+
+    def rewind(self, n_segments: int):
+        _check(lib().qwm_rewind(self._h, int(n_segments)), "qwm_rewind")
+
+    def status(self) -> int:
+        return lib().qwm_get_status(self._h, _stream())
+
+    def status_bits(self) -> int:
+        b = ctypes.c_uint32(0)
+        _check(lib().qwm_peek_status_bits(self._h, ctypes.byref(b), _stream()), "qwm_peek_status_bits")
+        return int(b.value)
+
+    def set_attend_kernel(self, k: int):
+        _check(lib().qwm_set_attend_kernel(self._h, int(k)), "qwm_set_attend_kernel")
+
+    @property
+    def resolved_attend_kernel(self) -> int:
+        return int(lib().qwm_resolved_attend_kernel(self._h))
+
+    @property
+    def n_tokens(self) -> int:
+        return int(lib().qwm_num_tokens(self._h))
+
+    @property
+    def n_tiles(self) -> int:
+        return int(lib().qwm_num_tiles(self._h))
+
+    @property
+    def n_segments(self) -> int:
+        return int(lib().qwm_num_segments(self._h))
+
+    @property
+    def version(self) -> int:
+        return int(lib().qwm_version(self._h))
+
+    def cache_tiles(self) -> torch.Tensor:
+        """View of the cache as [H, max_tiles, tile_bytes] uint8."""
+        L = self.layout
+        return self.cache[: L.cache_bytes].view(self.cfg.heads, L.max_tiles, L.tile_bytes)
+
+    def tile_table(self) -> torch.Tensor:
+        """View of the tile table as [max_tiles, 2] int32 (basis version, valid slots)."""
+        L = self.layout
+        return self.state[L.st_tiles: L.st_tiles + 8 * L.max_tiles].view(torch.int32).view(L.max_tiles, 2)
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().qwm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

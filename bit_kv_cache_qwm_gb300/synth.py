@@ -192,17 +192,30 @@ def hist_queries(wl: Workload, step: int = 0, heads: Sequence[int] | None = None
     """Historical queries used to calibrate before step `step`: float32 [heads, n_h, d].
 
     Streaming workloads keep a ring of the most recent n_h queries of earlier
-    chunks; before the first step the ring is a seeded draw of its own.
+    chunks; before the first step the ring is a seeded draw of its own.  Other
+    workloads draw a fresh seeded set for every `step`.
     """
     if wl.steps and step > 0:
         q = queries(wl, step - 1, heads)
         return np.ascontiguousarray(q[:, -wl.n_hist:, :])
-    return _stack(_qhist1, heads, wl, 0, wl.n_hist)
+    return _stack(_qhist1, heads, wl, step, wl.n_hist)
 
 
 def kmeans_init_rows(wl: Workload, head: int, n_frame: int, n_centroids: int) -> np.ndarray:
     """Seeded choice of distinct rows of frame 0 that start Lloyd's iteration."""
     return _rng(wl, _KMINIT, head).permutation(n_frame)[:n_centroids].astype(np.int64)
+
+
+def kmeans_keys(wl: Workload, heads: Sequence[int] | None = None) -> np.ndarray:
+    """The keys of frame 0 that the centroids are fitted on: the first
+    `kmeans_tokens` keys appended, float32 [heads, kmeans_tokens, d]."""
+    parts, got, ch = [], 0, 0
+    while got < wl.kmeans_tokens:
+        n = min(wl.chunk, wl.kmeans_tokens - got)
+        parts.append(keys(wl, ch, heads, n))
+        got += n
+        ch += 1
+    return np.concatenate(parts, axis=1)
 
 
 def workload(name: str) -> Workload:

@@ -1,0 +1,192 @@
+/*
+ * libqwm -- the QuantWM 2-bit KV cache on one GB300 GPU (sm_103a).
+ *
+ * C ABI of the data-parallel hot path of QuantWM ("QuantWM: Temporally
+ * Consistent 2-Bit KV Cache Quantization for World Models and Video
+ * Generation", Abstract; the roboind article on QuantWM, sections "Step 1" and
+ * "Step 2"):
+ *
+ *   qwm_calibrate  historical-query sensitivity s_c = mean q_c^2 and the PSAC
+ *                  basis U_r (top-r eigenvectors of Q_hist^T Q_hist);
+ *   qwm_append     QSAC centroid choice, INT2 quantisation and 2-bit packing of
+ *                  the key residual and of the value, PSAC coefficients
+ *                  e = U_r (k - k_hat);
+ *   qwm_attend     softmax attention of a query chunk over every cached token,
+ *                  logit = q.k_hat + (q U_r^T).e.
+ *
+ * Conventions shared by every call
+ *   - The caller owns every device buffer (cache, state, workspace, inputs,
+ *     outputs); the library owns only the host handle qwm_ctx.
+ *   - Device pointers are plain CUDA device addresses on the device that was
+ *     current at qwm_create.  Tensors are dense and row-major:
+ *     keys, values, queries and outputs are [heads][rows][head_dim] in the
+ *     configured dtype (float32 or bfloat16).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Compute calls are asynchronous on that stream; calls on one
+ *     context must be ordered (one stream, or events between streams).
+ *   - Errors found on the host (arguments, sizes, capacity, call order) are
+ *     returned before any launch and leave the context unchanged.  A CUDA
+ *     launch error returns QWM_ERR_CUDA.  Conditions found on the device (an
+ *     eigen-solver that did not converge, a float16 parameter that saturated)
+ *     set bits of a device status word read by qwm_get_status.
+ *   - Every entry point is thread-compatible: one context must not be used by
+ *     two host threads at once.
+ */
+#ifndef QWM_H
+#define QWM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QWM_OK = 0,
+  QWM_ERR_INVALID_ARG = 1,     /* null pointer, bad size or shape             */
+  QWM_ERR_UNSUPPORTED = 2,     /* valid but not built (e.g. head_dim 96)      */
+  QWM_ERR_CAPACITY = 3,        /* cache tiles or basis versions exhausted     */
+  QWM_ERR_NOT_CALIBRATED = 4,  /* append/attend before calibrate/centroids    */
+  QWM_ERR_NOT_CONVERGED = 5,   /* device: eigen-solver hit its iteration cap  */
+  QWM_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed        */
+  QWM_ERR_OOM = 7,             /* host allocation failed                      */
+  QWM_ERR_DEVICE = 8           /* device: other status bits set (see below)   */
+} qwm_status;
+
+typedef enum { QWM_F32 = 0, QWM_BF16 = 1 } qwm_dtype;
+
+/* device status word bits (qwm_get_status / qwm_peek_status_bits) */
+#define QWM_DEV_NOT_CONVERGED 0x1u  /* calibrate: residual above tolerance at max_iter */
+#define QWM_DEV_SATURATED     0x2u  /* append: a float16 zero or scale saturated at 65504 */
+
+typedef struct {
+  int32_t heads;         /* H >= 1                                              */
+  int32_t head_dim;      /* d: 64 or 128                                        */
+  int32_t group;         /* channels per quantisation group: must be 32         */
+  int32_t rank;          /* PSAC rank r, 0 <= r <= d                            */
+  int32_t n_centroids;   /* C, 1 <= C <= 1024                                   */
+  int32_t dtype;         /* qwm_dtype of keys, values, queries, centroids, out  */
+  int64_t max_tokens;    /* cache capacity in token slots (rounded up to 128);
+                            every append starts a new 128-slot tile             */
+  int32_t max_versions;  /* basis versions kept alive at once (>= 1)            */
+  int32_t max_iter;      /* eigen-solver iteration cap (>= 1)                   */
+  int32_t oversample;    /* extra subspace columns of the eigen-solver (>= 0)   */
+  int32_t max_hist;      /* largest n_h a calibrate call may pass (>= 1)        */
+} qwm_config;
+
+/* Sizes and byte offsets derived from a config (qwm_sizes). */
+typedef struct {
+  size_t cache_bytes;      /* H * max_tiles * tile_bytes                        */
+  size_t state_bytes;      /* calibration, centroids, bases, tile table, status */
+  size_t workspace_bytes;  /* calibrate scratch                                 */
+  size_t tile_bytes;       /* bytes of one 128-slot tile of one head            */
+  size_t bytes_per_token;  /* tile_bytes / 128                                  */
+  int64_t max_tiles;       /* tiles per head                                    */
+  /* offsets of the sections inside one tile */
+  size_t off_idx, off_kcode, off_kqp, off_e, off_vcode, off_vqp;
+  /* offsets of the arrays inside the state buffer */
+  size_t st_status, st_s, st_w, st_lambda, st_energy, st_centroids, st_basis, st_tiles, st_iters;
+} qwm_layout;
+
+typedef struct qwm_ctx qwm_ctx;
+
+/* Human-readable name of a status code (static string). */
+const char* qwm_status_string(qwm_status s);
+
+/* Validate `cfg` and compute every size and offset.  No CUDA call.
+ * Cache layout: [H][max_tiles][tile_bytes]; one tile holds 128 token slots as
+ *   idx   u8 (C <= 256) or u16       [128]
+ *   kcode 2-bit K residual codes     [128][d/4]   channel c in byte c/4, bits 2(c%4)
+ *   kqp   fp16 (zero, scale) of K    [128][d/32][2]
+ *   e     fp16 PSAC coefficients     [128][r]
+ *   vcode 2-bit V codes              [128][d/4]
+ *   vqp   fp16 (zero, scale) of V    [128][d/32][2]
+ * State tile table: int32 pairs (basis version, valid slots) per tile. */
+qwm_status qwm_sizes(const qwm_config* cfg, qwm_layout* out);
+
+/* Bind a context to caller-owned device buffers of at least the sizes from
+ * qwm_sizes (256-byte aligned).  Zeroes the state buffer (synchronously).
+ * The buffers must outlive the context.  *out receives the handle. */
+qwm_status qwm_create(const qwm_config* cfg, void* d_cache, void* d_state, void* d_workspace,
+                      qwm_ctx** out);
+
+/* Release the host handle (device buffers stay with the caller). NULL is a no-op. */
+qwm_status qwm_destroy(qwm_ctx* ctx);
+
+/* Copy the high-precision centroids [H][C][d] (configured dtype, device) into
+ * the state.  QSAC chooses among these ("each Key is assigned to a
+ * clustering center ... the center retaining high accuracy", roboind
+ * article, "Step 1").  Asynchronous on `stream`. */
+qwm_status qwm_set_centroids(qwm_ctx* ctx, const void* d_centroids, void* stream);
+
+/* Calibrate from n_h historical queries [H][n_h][d] (device, configured dtype):
+ * s_c = mean q_c^2, group weights w_g = sum of s over the group, and the PSAC
+ * basis U_r = top-r eigenvectors of Q_hist^T Q_hist (rows, descending
+ * eigenvalue; the largest-magnitude entry of each is positive) by block
+ * subspace iteration with Rayleigh-Ritz ("the energy of historical queries
+ * tends to be concentrated in a few directions", roboind article "Step 2").
+ * Opens a new basis version: later appends store coefficients in it.
+ * Needs 1 <= n_h <= max_hist.  Asynchronous; non-convergence within max_iter
+ * sets QWM_DEV_NOT_CONVERGED and keeps the best basis found. */
+qwm_status qwm_calibrate(qwm_ctx* ctx, const void* d_q_hist, int64_t n_h, void* stream);
+
+/* Install a calibration computed elsewhere: s [H][d] and U [H][r][d] (host
+ * float32).  Opens a new basis version like qwm_calibrate.  Synchronous. */
+qwm_status qwm_set_calibration(qwm_ctx* ctx, const float* h_s, const float* h_U, void* stream);
+
+/* Read the current calibration back (host float32, any pointer may be NULL):
+ * s [H][d], U [H][r][d], lambda [H][r], energy [H] = sum(lambda)/trace.
+ * Synchronous. */
+qwm_status qwm_get_calibration(qwm_ctx* ctx, float* h_s, float* h_U, float* h_lambda,
+                               float* h_energy, void* stream);
+
+/* Append one chunk of n tokens: keys and values [H][n][d] (device).  For each
+ * key: QSAC j* = argmin_j sum_g w_g (range_g(k - C_j)/3)^2/12 (float32
+ * decision, lowest j on a tie), the residual k - C_j* and the value are
+ * quantised per 32-channel group to INT2 with fp16 zero = min and
+ * scale = range/3, packed 4 codes a byte, and e = U_r (k - k_hat) is stored
+ * as r fp16 values (QuantWM Abstract; roboind article "Step 1", "Step 2").
+ * Occupies ceil(n/128) new tiles; slots past n in the last tile are zeroed
+ * and masked in attention.  n = 0 is a no-op.  Needs a calibration and
+ * centroids.  Asynchronous. */
+qwm_status qwm_append(qwm_ctx* ctx, const void* d_k, const void* d_v, int64_t n, void* stream);
+
+/* Attention of M query rows [H][M][d] over every cached token:
+ *   O = softmax(scale * (q.k_hat_n + (q U_t(n)^T).e_n)) V_hat
+ * with U_t(n) the basis version the token was appended under ("the current
+ * Query matching score with the Historical Key determines how the model
+ * allocates attention", roboind article, "The key to a smaller error").
+ * softmax_scale <= 0 selects 1/sqrt(d).  Output [H][M][d] in the configured
+ * dtype (device).  The cache must hold at least one token.  Asynchronous. */
+qwm_status qwm_attend(qwm_ctx* ctx, const void* d_q, int64_t M, float softmax_scale, void* d_out,
+                      void* stream);
+
+/* Drop every segment (append call) after the first n_segments, freeing their
+ * tiles.  Host bookkeeping only; no device work. */
+qwm_status qwm_rewind(qwm_ctx* ctx, int32_t n_segments);
+
+/* Synchronise `stream`, read and clear the device status word.  Returns
+ * QWM_ERR_NOT_CONVERGED or QWM_ERR_DEVICE when bits were set, else QWM_OK. */
+qwm_status qwm_get_status(qwm_ctx* ctx, void* stream);
+
+/* Same as qwm_get_status but returns the raw bits in *bits. */
+qwm_status qwm_peek_status_bits(qwm_ctx* ctx, uint32_t* bits, void* stream);
+
+/* Attention kernel choice: 0 = automatic (tensor-core kernel where it
+ * applies), 1 = float32 CUDA-core kernel, 2 = bf16 mma.sync kernel,
+ * 3 = bf16 tcgen05 kernel. */
+qwm_status qwm_set_attend_kernel(qwm_ctx* ctx, int32_t kernel);
+
+/* The attention kernel qwm_attend will run (1, 2 or 3; automatic resolved). */
+int32_t qwm_resolved_attend_kernel(const qwm_ctx* ctx);
+
+int64_t qwm_num_tokens(const qwm_ctx* ctx);    /* valid tokens cached        */
+int64_t qwm_num_tiles(const qwm_ctx* ctx);     /* tiles in use per head      */
+int32_t qwm_num_segments(const qwm_ctx* ctx);  /* append calls kept          */
+int32_t qwm_version(const qwm_ctx* ctx);       /* current basis version, -1 before any */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QWM_H */
