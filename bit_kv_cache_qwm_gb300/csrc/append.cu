@@ -250,7 +250,7 @@ cudaError_t launch_t(const qwm_ctx* c, const void* k, const void* v, int64_t n, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((n + kTile - 1) / kTile), (unsigned)H);
-  const float* U = c->basis + (size_t)(version % c->cfg.max_versions) * H * r * D;
+  const float* U = c->basis + (size_t)version * H * r * D;   // version = basis slot
   kern<<<grid, kTile * (D / kGroup), smem, st>>>(
       (const T*)k, (const T*)v, n, (const T*)c->centroids, nC, c->w, U, r, c->cache,
       c->lay.max_tiles, tile_offsets(c->lay), tile0, version, c->tiles, c->status, c->ib);

@@ -95,7 +95,7 @@ attend_simt_kernel(const T* __restrict__ Q, int64_t M, float scale, T* __restric
     // ---- q U^T for a new basis version ----
     if (meta.x != cur_version && r > 0) {
       cur_version = meta.x;
-      const float* U = basis + ((int64_t)(cur_version % max_versions) * H + h) * r * D;
+      const float* U = basis + ((int64_t)cur_version * H + h) * r * D;
       for (int i = threadIdx.x; i < kRows * r; i += blockDim.x) {
         const int a = i / r, m = i % r;
         double s = 0.0;

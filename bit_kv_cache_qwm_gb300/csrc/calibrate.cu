@@ -499,7 +499,7 @@ cudaError_t launch_eig(const qwm_ctx* c, int64_t n_h, int32_t version, cudaStrea
   const size_t bytes = L.floats * 4;
   const int use_smem = bytes <= 160 * 1024;
   const size_t smem = use_smem ? bytes : 0;
-  float* U = c->basis + (size_t)(version % c->cfg.max_versions) * H * (r > 0 ? r : 1) * D;
+  float* U = c->basis + (size_t)version * H * (r > 0 ? r : 1) * D;   // version = basis slot
   const int sp = splits_for(n_h);
   cudaError_t e;
   if (D == 128) {

@@ -119,6 +119,7 @@ extern "C" qwm_status qwm_create(const qwm_config* c, void* d_cache, void* d_sta
   x->n_tokens = 0;
   x->n_tiles = 0;
   x->version = -1;
+  x->slot = -1;
   x->centroids_set = false;
   x->attend_kernel = 0;
   if (cudaMemset(d_state, 0, L.state_bytes) != cudaSuccess ||
@@ -144,40 +145,46 @@ extern "C" qwm_status qwm_set_centroids(qwm_ctx* x, const void* d_centroids, voi
   return QWM_OK;
 }
 
-// A new basis version may reuse slot (v % max_versions) only if no live
-// segment still refers to the version that held it before.
-static qwm_status next_version(qwm_ctx* x, int32_t* v_out) {
-  int32_t v = x->version + 1;
-  for (const auto& s : x->segs)
-    if (s.version <= v - x->cfg.max_versions) return QWM_ERR_CAPACITY;
-  *v_out = v;
-  return QWM_OK;
+// A new basis version takes the lowest basis slot that neither the current
+// version nor any live segment uses; with none free the call fails.
+static qwm_status next_version(qwm_ctx* x, int32_t* v_out, int32_t* slot_out) {
+  for (int32_t s = 0; s < x->cfg.max_versions; ++s) {
+    bool used = (x->version >= 0 && x->slot == s);
+    for (const auto& g : x->segs) used = used || g.slot == s;
+    if (!used) {
+      *v_out = x->version + 1;
+      *slot_out = s;
+      return QWM_OK;
+    }
+  }
+  return QWM_ERR_CAPACITY;
 }
 
 extern "C" qwm_status qwm_calibrate(qwm_ctx* x, const void* d_q, int64_t n_h, void* stream) {
   if (!x || !d_q || n_h < 1 || n_h > x->cfg.max_hist) return QWM_ERR_INVALID_ARG;
-  int32_t v;
-  qwm_status st = next_version(x, &v);
+  int32_t v, slot;
+  qwm_status st = next_version(x, &v, &slot);
   if (st != QWM_OK) return st;
   cudaError_t e = launch_gram(x, d_q, n_h, S(stream));
-  if (e == cudaSuccess) e = launch_eig(x, n_h, v, S(stream));
+  if (e == cudaSuccess) e = launch_eig(x, n_h, slot, S(stream));
   if (e == cudaSuccess) e = launch_group_weights(x, S(stream));
   if (e != cudaSuccess) return QWM_ERR_CUDA;
   x->version = v;
+  x->slot = slot;
   return QWM_OK;
 }
 
 extern "C" qwm_status qwm_set_calibration(qwm_ctx* x, const float* h_s, const float* h_U,
                                           void* stream) {
   if (!x || !h_s || (x->cfg.rank > 0 && !h_U)) return QWM_ERR_INVALID_ARG;
-  int32_t v;
-  qwm_status st = next_version(x, &v);
+  int32_t v, slot;
+  qwm_status st = next_version(x, &v, &slot);
   if (st != QWM_OK) return st;
   const size_t H = x->cfg.heads, d = x->cfg.head_dim, r = x->cfg.rank;
   cudaStream_t s = S(stream);
   cudaError_t e = cudaMemcpyAsync(x->s, h_s, H * d * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && r > 0) {
-    float* dst = x->basis + (size_t)(v % x->cfg.max_versions) * H * r * d;
+    float* dst = x->basis + (size_t)slot * H * r * d;
     e = cudaMemcpyAsync(dst, h_U, H * r * d * 4, cudaMemcpyHostToDevice, s);
   }
   if (e == cudaSuccess) e = cudaMemsetAsync(x->lambda, 0, H * (r > 0 ? r : 1) * 4, s);
@@ -186,6 +193,7 @@ extern "C" qwm_status qwm_set_calibration(qwm_ctx* x, const float* h_s, const fl
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return QWM_ERR_CUDA;
   x->version = v;
+  x->slot = slot;
   return QWM_OK;
 }
 
@@ -198,7 +206,7 @@ extern "C" qwm_status qwm_get_calibration(qwm_ctx* x, float* h_s, float* h_U, fl
   cudaError_t e = cudaSuccess;
   if (h_s) e = cudaMemcpyAsync(h_s, x->s, H * d * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess && h_U && r > 0)
-    e = cudaMemcpyAsync(h_U, x->basis + (size_t)(x->version % x->cfg.max_versions) * H * r * d,
+    e = cudaMemcpyAsync(h_U, x->basis + (size_t)x->slot * H * r * d,
                         H * r * d * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess && h_lambda && r > 0)
     e = cudaMemcpyAsync(h_lambda, x->lambda, H * r * 4, cudaMemcpyDeviceToHost, s);
@@ -216,13 +224,14 @@ extern "C" qwm_status qwm_append(qwm_ctx* x, const void* d_k, const void* d_v, i
   if (x->version < 0 || !x->centroids_set) return QWM_ERR_NOT_CALIBRATED;
   const int64_t tiles = (n + kTile - 1) / kTile;
   if (x->n_tiles + tiles > x->lay.max_tiles) return QWM_ERR_CAPACITY;
-  cudaError_t e = launch_append(x, d_k, d_v, n, x->n_tiles, x->version, S(stream));
+  cudaError_t e = launch_append(x, d_k, d_v, n, x->n_tiles, x->slot, S(stream));
   if (e != cudaSuccess) return QWM_ERR_CUDA;
   SegmentRec r;
   r.first_tile = x->n_tiles;
   r.n_tiles = tiles;
   r.n_tokens = n;
   r.version = x->version;
+  r.slot = x->slot;
   x->segs.push_back(r);
   x->n_tiles += tiles;
   x->n_tokens += n;

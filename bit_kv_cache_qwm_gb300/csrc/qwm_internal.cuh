@@ -20,6 +20,7 @@ struct SegmentRec {
   int64_t n_tiles;
   int64_t n_tokens;
   int32_t version;
+  int32_t slot;     // basis slot holding that version's U
 };
 
 }  // namespace qwm
@@ -48,6 +49,7 @@ struct qwm_ctx {
   int64_t n_tokens;
   int64_t n_tiles;
   int32_t version;       // -1 before the first calibration
+  int32_t slot;          // basis slot of the current version
   bool centroids_set;
   int32_t attend_kernel;
   std::vector<qwm::SegmentRec> segs;

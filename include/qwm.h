@@ -69,7 +69,8 @@ typedef struct {
   int32_t dtype;         /* qwm_dtype of keys, values, queries, centroids, out  */
   int64_t max_tokens;    /* cache capacity in token slots (rounded up to 128);
                             every append starts a new 128-slot tile             */
-  int32_t max_versions;  /* basis versions kept alive at once (>= 1)            */
+  int32_t max_versions;  /* basis slots: versions alive at once, the current
+                            one included (>= 1)                                 */
   int32_t max_iter;      /* eigen-solver iteration cap (>= 1)                   */
   int32_t oversample;    /* extra subspace columns of the eigen-solver (>= 0)   */
   int32_t max_hist;      /* largest n_h a calibrate call may pass (>= 1)        */
@@ -102,7 +103,8 @@ const char* qwm_status_string(qwm_status s);
  *   e     fp16 PSAC coefficients     [128][r]
  *   vcode 2-bit V codes              [128][d/4]
  *   vqp   fp16 (zero, scale) of V    [128][d/32][2]
- * State tile table: int32 pairs (basis version, valid slots) per tile. */
+ * State tile table: int32 pairs (basis slot, valid slots) per tile; a basis
+ * slot holds the U of one live basis version. */
 qwm_status qwm_sizes(const qwm_config* cfg, qwm_layout* out);
 
 /* Bind a context to caller-owned device buffers of at least the sizes from

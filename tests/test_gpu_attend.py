@@ -117,7 +117,7 @@ def test_full_rank_compensation_on_gpu(qwm, kernel):
     assert np.abs(got - want).max() <= 1e-5 * vmax
 
 
-@pytest.mark.parametrize("kernel", [1])
+@pytest.mark.parametrize("kernel", [1, 2])
 def test_attend_bf16_sampled_rows(qwm, kernel):
     """12 heads over 3 appends; the oracle checks every row of heads 0 and 9."""
     name = "bf16-h12-n32760"
@@ -127,3 +127,52 @@ def test_attend_bf16_sampled_rows(qwm, kernel):
     got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
     want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, q, [0, 9], 1 / np.sqrt(128))
     assert np.abs(got[[0, 9]] - want).max() <= 1e-2 * vmax
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("name,C,r", [("bf16-h12-n32760", 256, 16), ("bf16-h24-append-sweep", 1024, 32),
+                                      ("bf16-h24-append-sweep", 64, 8), ("bf16-h24-append-sweep", 256, 0),
+                                      ("bf16-h40-n98280-outlier", 256, 16)])
+def test_attend_bf16_variants(qwm, kernel, name, C, r):
+    """Ragged appends (tails of 1 and 100 slots), three basis versions, rank
+    0 / 8 / 16 / 32, centroids staged in shared memory (C <= 256) or read
+    from global memory (C = 1024), outlier channels, M = 200 (two row blocks,
+    ragged)."""
+    wl = synth.workload(name)
+    heads = [0, 1]
+    cent = centroids(name, tuple(heads), C, iters=25 if C <= 256 else 3)
+    sizes = [300, 1, 228, 129, 100, 64]
+    ctx = qwm.Qwm(2, 128, r, C, dtype="bf16", max_tokens=sum((n + 127) // 128 for n in sizes) * 128,
+                  max_versions=3)
+    ctx.set_centroids(_tensor(cent, "bf16"))
+    bases = []
+    for ch, n in enumerate(sizes):
+        if ch % 2 == 0:
+            s_, U = calibration(name, tuple(heads), r, step=len(bases))
+            ctx.set_calibration(s_, U)
+            bases.append(U)
+        ctx.append(_tensor(synth.keys(wl, ch, heads, n), "bf16"), _tensor(synth.values(wl, ch, heads, n), "bf16"))
+    ctx.set_attend_kernel(kernel)
+    q = synth.queries(wl, 3, heads, m=200)
+    got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
+    want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, q, [0, 1], 1 / np.sqrt(128))
+    err = np.abs(got - want).max()
+    assert err <= 1e-2 * vmax, (err, vmax)
+
+
+def test_attend_full_size_bench_configuration(qwm):
+    """The benchmarked workload at full size in the launch configuration the
+    benchmark times (automatic kernel choice): 12 heads, 7 appends of 4,680
+    tokens (32,760 cached), 4,680 query rows.  The oracle recomputes 48 seeded
+    rows of heads 0 and 11 over the GPU's cache bytes."""
+    name = "bf16-h12-n32760"
+    wl, ctx, cent, bases = _build(qwm, name, list(range(12)), [wl_chunk for wl_chunk in [4680] * 7])
+    q = synth.queries(wl, 0)
+    got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
+    assert ctx.resolved_attend_kernel == 2
+    rows = np.sort(np.random.default_rng(5).choice(wl.n_query, 48, replace=False))
+    qs = q[:, rows]
+    want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, qs, [0, 11], 1 / np.sqrt(128))
+    err = np.abs(got[[0, 11]][:, rows] - want).max()
+    assert err <= 1e-2 * vmax, (err, vmax)
+    assert np.isfinite(got).all()
