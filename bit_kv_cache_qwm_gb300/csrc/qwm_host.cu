@@ -145,11 +145,13 @@ extern "C" qwm_status qwm_set_centroids(qwm_ctx* x, const void* d_centroids, voi
   return QWM_OK;
 }
 
-// A new basis version takes the lowest basis slot that neither the current
-// version nor any live segment uses; with none free the call fails.
+// A new basis version takes the lowest basis slot that no live segment uses;
+// with none free the call fails.  The current version's slot may be taken
+// when no segment refers to it: the new basis replaces it, and an append
+// still reading it is ordered before the overwrite on the caller's stream.
 static qwm_status next_version(qwm_ctx* x, int32_t* v_out, int32_t* slot_out) {
   for (int32_t s = 0; s < x->cfg.max_versions; ++s) {
-    bool used = (x->version >= 0 && x->slot == s);
+    bool used = false;
     for (const auto& g : x->segs) used = used || g.slot == s;
     if (!used) {
       *v_out = x->version + 1;

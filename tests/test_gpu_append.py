@@ -117,20 +117,25 @@ def test_host_side_errors(qwm):
     assert e.value.status == 4                     # not calibrated
     ctx.set_centroids(_tensor(centroids(wl.name), "f32"))
     s, U = calibration(wl.name)
-    ctx.set_calibration(s, U)
+    ctx.set_calibration(s, U)                      # version 0 in slot 0
+    ctx.set_calibration(s, U)                      # version 1 reuses slot 0 (no segment uses it)
     ctx.append(k, k)
+    ctx.set_calibration(s, U)                      # version 2 in slot 1
     ctx.append(k, k)
     with pytest.raises(qwm.QwmError) as e:
-        ctx.append(k, k)                           # third tile does not fit in 256 slots
+        ctx.append(k, k)                           # a third tile does not fit in 256 slots
     assert e.value.status == 3
     assert ctx.n_tokens == 256 and ctx.n_segments == 2
-    ctx.set_calibration(s, U)                      # version 1
     with pytest.raises(qwm.QwmError) as e:
-        ctx.set_calibration(s, U)                  # would overwrite version 0 still in use
+        ctx.set_calibration(s, U)                  # both slots hold live segments
     assert e.value.status == 3
+    assert ctx.version == 2
+    table = ctx.tile_table().cpu().numpy()
+    assert table[:2, 0].tolist() == [0, 1]
+    ctx.rewind(1)                                  # drops the version-2 segment
+    ctx.set_calibration(s, U)                      # version 3 takes slot 1
+    assert ctx.version == 3 and ctx.n_tokens == 128
     ctx.rewind(0)
-    ctx.set_calibration(s, U)                      # version 0 no longer referenced
-    assert ctx.version == 2 and ctx.n_tokens == 0
     with pytest.raises(qwm.QwmError) as e:
         ctx.attend(_tensor(synth.queries(wl, 0), "f32"))
     assert e.value.status == 1                     # empty cache
