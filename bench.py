@@ -42,6 +42,22 @@ def attend_flops(H, M, N, d, r):
     return H * (4.0 * M * N * d + 2.0 * M * N * r + 2.0 * M * d * r)
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over all ranks (the step time that bounds the job)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, world: int, max_ms: float) -> float:
+    """Work of all replicas divided by the slowest rank's step time."""
+    return world * flops_per_rank_step / (max_ms * 1e-3) / 1e12
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -268,11 +284,7 @@ def run_gpu(args):
     app = [e[1].elapsed_time(e[2]) for e in evs]
     att = [e[2].elapsed_time(e[3]) for e in evs]
     stp = [e[0].elapsed_time(e[3]) for e in evs]
-    ms_step = float(np.mean(stp))
-    if world > 1:
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = max_over_ranks(float(np.mean(stp)), dev)
 
     # end to end through the public API with host buffers (pinned), copies timed
     h_qh, h_k, h_v, h_q = (x.cpu().pin_memory() for x in (qh, k_new, v_new, q))
@@ -303,7 +315,7 @@ def run_gpu(args):
     peaks = load_peaks()
     att_ms = float(np.mean(att))
     achieved = flops / (att_ms * 1e-3) / 1e12
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, ms_step)
     kernel = {0: "auto", 1: "simt", 2: "mma", 3: "tcgen05"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
