@@ -231,6 +231,7 @@ def run_gpu(args):
     if args.kmeans and hasattr(ctx, "kmeans"):
         cent = ctx.kmeans(T(kf), cent, iters=25)
     ctx.set_centroids(cent)
+    ctx.set_attend_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3}[args.kernel])
     qh = T(synth.hist_queries(wl, 0))
     ctx.calibrate(qh)
     for ch in range(n_prefix):
@@ -363,6 +364,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kmeans", action="store_true", default=True)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma", "tc"],
+                    help="attention kernel (auto picks the fastest that applies)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

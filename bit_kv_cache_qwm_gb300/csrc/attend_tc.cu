@@ -1,0 +1,586 @@
+// qwm_attend, sm_103a tensor-core kernel: tcgen05.mma with TMEM accumulators.
+//
+// Attention over the packed cache with PSAC compensation (QuantWM Abstract;
+// roboind article, "Step 2"):
+//   l_n = q . k_hat_n + (q U_t^T) . e_n,   O = softmax(scale * l) V_hat.
+//
+// One CTA owns 128 query rows of one head and streams every 128-slot tile of
+// that head.  Warp roles:
+//   warps 0-3   softmax: thread i owns query row i (TMEM lane i).  Reads S
+//               from TMEM, online softmax in the exp2 domain with a lazy
+//               rescale (O is corrected only when the running maximum grows
+//               by more than 2^8), writes P (fp16) into TMEM, final 1/l and
+//               store of O.
+//   warps 4-11  producers: load Q once (SW128 K-major smem), and per tile
+//               dequantise k_hat into two bf16 terms (hi + lo, SW128 K-major,
+//               rows = keys), v_hat^T into fp16 (SW128 K-major, rows = d), e
+//               into a no-swizzle K-major fp16 tile; recompute Z = q U_t^T as
+//               two fp16 terms when the tile's basis slot changes.
+//   warp 12     MMA issuer (one lane) and TMEM owner:
+//               S[t&1]  = Q khi^T + Q klo^T + Zhi E^T + Zlo E^T   (M=128, N=128)
+//               O      += P V_hat                                 (A = P in TMEM)
+//               S(t+1) is issued before PV(t) so the tensor core works while
+//               the softmax warps handle tile t.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P [384,448).
+// Synchronisation: mbarriers (k_ready, v_ready, p_ready, s_free[2] arrived by
+// threads; s_done[2], pv_done by tcgen05.commit).  Every wait is bounded by
+// the SM clock; a timeout sets a device status bit and every role leaves its
+// loop, the TMEM is freed and the kernel returns.
+#include <math.h>
+
+#include "qwm_internal.cuh"
+
+namespace qwm {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kSoftWarps = 4, kProdWarps = 8;
+constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;   // 416
+constexpr int kProdThreads = kProdWarps * 32;
+constexpr uint32_t kColS0 = 0, kColO = 256, kColP = 384;
+constexpr long long kWaitCycles = 1ll << 31;                    // ~1 s at 2 GHz
+constexpr uint32_t kDevTimeout = 0x4u;
+
+constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | (16u << 17) | (8u << 24);  // bf16 x bf16 -> f32
+constexpr uint32_t kIdescF16 = (1u << 4) | (16u << 17) | (8u << 24);                           // f16 x f16 -> f32
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+// no-swizzle K-major: core matrices of 8 rows x 16 B; lbo = next core along K,
+// sbo = next core along M/N
+__device__ __forceinline__ uint64_t desc_none(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         (1ull << 46);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+               ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+               "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+               ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
+}
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(su32(bar)) : "memory");
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+  asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(su32(b)) : "memory");
+}
+// Bounded wait for the completion of the phase with parity `par`.  Returns
+// false (after flagging) on timeout or when another role already gave up.
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t par, volatile int* abort_flag,
+                                         uint32_t* status) {
+  const long long t0 = clock64();
+  while (true) {
+    uint32_t done;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                 "selp.u32 %0, 1, 0, p;\n}"
+                 : "=r"(done) : "r"(su32(b)), "r"(par) : "memory");
+    if (done) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      atomicOr(status, kDevTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+               "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                 "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+                 "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+                 "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+                 "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+               "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+               ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+                 "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]),
+                 "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+                 "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+               "%14,%15,%16};"
+               ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+                 "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
+                 "r"(v[14]), "r"(v[15])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void prod_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kProdThreads) : "memory"); }
+
+// byte offset of (row, k) in a [128 rows][128 k] 16-bit tile stored as two
+// SW128 K-major atoms of 64 k each (chunk = 8 elements)
+__device__ __forceinline__ int sw128_off(int row, int chunk16) {
+  return (chunk16 >> 3) * 16384 + (row >> 3) * 1024 + (row & 7) * 128 + (((chunk16 & 7) ^ (row & 7)) << 4);
+}
+// centroid rows in smem: [C][256 B], 16-byte chunks XOR-swizzled by row & 7
+__device__ __forceinline__ int cswz(int row, int chunk) { return row * 256 + ((chunk ^ (row & 7)) << 4); }
+
+struct TcArgs {
+  const __nv_bfloat16* Q;
+  __nv_bfloat16* O;
+  int64_t M;
+  float scale_log2;
+  const uint8_t* cache;
+  int64_t max_tiles;
+  TileOffsets off;
+  int64_t n_tiles;
+  const int2* tiles;
+  const __nv_bfloat16* cent;
+  int nC;
+  const float* basis;
+  int H;
+  int r;
+  int ib;
+  uint32_t* status;
+};
+
+template <int RP, bool CS>
+__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) {
+  constexpr int G = kD / kGroup;
+  extern __shared__ __align__(1024) uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((1024 - (su32(sm_raw) & 1023)) & 1023);
+  uint8_t* Qs = sm;                      // 32 KB
+  uint8_t* Khi = sm + 32768;             // 32 KB
+  uint8_t* Klo = sm + 65536;             // 32 KB
+  uint8_t* Vt = sm + 98304;              // 32 KB
+  uint8_t* Es = sm + 131072;             // 128 x RP fp16, core matrices
+  uint8_t* Zh = Es + 128 * RP * 2;       // 128 x RP fp16
+  uint8_t* Zl = Zh + 128 * RP * 2;
+  uint8_t* Cs = Zl + 128 * RP * 2;       // C x 256 B (CS only)
+  __shared__ __align__(8) uint64_t bars[8];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_sh;
+  uint64_t* k_ready = &bars[0];
+  uint64_t* v_ready = &bars[1];
+  uint64_t* p_ready = &bars[2];
+  uint64_t* pv_done = &bars[3];
+  uint64_t* s_done = &bars[4];   // [2]
+  uint64_t* s_free = &bars[6];   // [2]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y;
+  const int64_t row0 = (int64_t)blockIdx.x * 128;
+  const int64_t nt = a.n_tiles;
+
+  if (tid == 0) {
+    abort_sh = 0;
+    bar_init(k_ready, kProdThreads);
+    bar_init(v_ready, kProdThreads);
+    bar_init(p_ready, 128);
+    bar_init(pv_done, 1);
+    bar_init(&s_done[0], 1);
+    bar_init(&s_done[1], 1);
+    bar_init(&s_free[0], 128);
+    bar_init(&s_free[1], 128);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 12) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&tmem_base_sh)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp < kSoftWarps) {
+    // ------------------------------------------------------------ softmax
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float c2 = a.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int64_t t = 0; t < nt && ok; ++t) {
+      const int b = (int)(t & 1);
+      const int nv = a.tiles[t].y;
+      if (!bar_wait(&s_done[b], (uint32_t)((t >> 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+      fence_after();
+      const uint32_t sbase = tmem + lane_base + kColS0 + 128u * b;
+      float mx = -INFINITY;
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t v[32];
+        tmem_ld32(sbase + 32 * cb, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (32 * cb + i < nv) mx = fmaxf(mx, __uint_as_float(v[i]));
+      }
+      const float mnew = fmaxf(m_run, mx * c2);
+      if (t > 0) {
+        if (!bar_wait(pv_done, (uint32_t)((t - 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+        fence_after();
+      }
+      if (mnew > m_run + 8.f) {
+        if (t > 0) {
+          const float corr = ex2(m_run - mnew);
+          for (int cb = 0; cb < 4; ++cb) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_base + kColO + 32 * cb, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+            tmem_st32(tmem + lane_base + kColO + 32 * cb, v);
+          }
+          l_run *= corr;
+        }
+        m_run = mnew;
+      }
+      float psum = 0.f;
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t v[32], pk[16];
+        tmem_ld32(sbase + 32 * cb, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int k0 = 32 * cb + 2 * i;
+          const float p0 = k0 < nv ? ex2(fmaf(__uint_as_float(v[2 * i]), c2, -m_run)) : 0.f;
+          const float p1 = k0 + 1 < nv ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), c2, -m_run)) : 0.f;
+          const __half2 hp = __floats2half2_rn(p0, p1);
+          const float2 back = __half22float2(hp);
+          psum += back.x + back.y;
+          pk[i] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        tmem_st16(tmem + lane_base + kColP + 16 * cb, pk);
+      }
+      tmem_wait_st();
+      l_run += psum;
+      fence_before();
+      bar_arrive(&s_free[b]);
+      bar_arrive(p_ready);
+    }
+    // epilogue
+    if (ok && nt > 0) ok = bar_wait(pv_done, (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+    fence_after();
+    const int64_t row = row0 + tid;
+    if (ok && row < a.M) {
+      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      __nv_bfloat16* dst = a.O + ((int64_t)h * a.M + row) * kD;
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kColO + 32 * cb, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 bb = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]) * inv,
+                                                            __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+            w[e] = *reinterpret_cast<const uint32_t*>(&bb);
+          }
+          *reinterpret_cast<uint4*>(dst + 32 * cb + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  } else if (warp < kSoftWarps + kProdWarps) {
+    // ------------------------------------------------------------ producers
+    const int p = tid - kSoftWarps * 32;      // 0..255
+    const __nv_bfloat16* ch = a.cent + (int64_t)h * a.nC * kD;
+    // Q rows into SW128 K-major smem: thread (row, half) copies 64 channels
+    {
+      const int row = p & 127, half = p >> 7;
+      const int64_t grow = row0 + row;
+      const __nv_bfloat16* src = a.Q + ((int64_t)h * a.M + grow) * kD + half * 64;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (grow < a.M) val = *reinterpret_cast<const uint4*>(src + 8 * c);
+        *reinterpret_cast<uint4*>(Qs + sw128_off(row, half * 8 + c)) = val;
+      }
+    }
+    if (CS) {
+      for (int i = p; i < a.nC * 16; i += kProdThreads) {
+        const int j = i >> 4, c = i & 15;
+        *reinterpret_cast<uint4*>(Cs + cswz(j, c)) = *reinterpret_cast<const uint4*>(ch + (int64_t)j * kD + 8 * c);
+      }
+    }
+    prod_sync();
+    int cur_slot = -1;
+    bool ok = true;
+    const uint8_t* tiles_h = a.cache + (int64_t)h * a.max_tiles * a.off.bytes;
+    for (int64_t t = 0; t < nt && ok; ++t) {
+      const uint8_t* tb = tiles_h + t * a.off.bytes;
+      const int slot = a.tiles[t].x;
+      if (t > 0) {
+        if (!bar_wait(&s_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+      }
+      if constexpr (RP > 0) {
+        if (slot != cur_slot) {
+          cur_slot = slot;
+          // stage U (fp32 [r][128]) in the free khi buffer, then Z = q U^T
+          float* Us = reinterpret_cast<float*>(Khi);
+          const float* U = a.basis + ((int64_t)slot * a.H + h) * a.r * kD;
+          for (int i = p; i < RP * kD; i += kProdThreads) Us[i] = (i / kD) < a.r ? U[i] : 0.f;
+          prod_sync();
+          if (p < 128) {
+            float z[RP];
+#pragma unroll
+            for (int i = 0; i < RP; ++i) z[i] = 0.f;
+            for (int c8 = 0; c8 < 16; ++c8) {
+              const uint4 qv = *reinterpret_cast<const uint4*>(Qs + sw128_off(p, c8));
+              const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const float qf = __uint_as_float(e & 1 ? (qw[e >> 1] & 0xffff0000u) : (qw[e >> 1] << 16));
+                const int c = 8 * c8 + e;
+#pragma unroll
+                for (int i = 0; i < RP; ++i) z[i] = fmaf(qf, Us[i * kD + c], z[i]);
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < RP / 8; ++j) {
+              uint32_t hw[4], lw[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __half h0 = __float2half_rn(z[8 * j + 2 * e]), h1 = __float2half_rn(z[8 * j + 2 * e + 1]);
+                const __half2 hh = __halves2half2(h0, h1);
+                const __half2 ll = __floats2half2_rn(z[8 * j + 2 * e] - __half2float(h0),
+                                                     z[8 * j + 2 * e + 1] - __half2float(h1));
+                hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                lw[e] = *reinterpret_cast<const uint32_t*>(&ll);
+              }
+              const int off = ((p >> 3) * (RP / 8) + j) * 128 + (p & 7) * 16;
+              *reinterpret_cast<uint4*>(Zh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(Zl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+          }
+          prod_sync();
+        }
+      }
+      // ---- k_hat (hi, lo) and e ----
+      {
+        const int key = p & 127, half = p >> 7;
+        const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
+        const uint4 kc = *reinterpret_cast<const uint4*>(tb + a.off.kcode + key * 32 + half * 16);
+        const uint2 kq = *reinterpret_cast<const uint2*>(tb + a.off.kqp + (key * G + 2 * half) * 4);
+        const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
+#pragma unroll
+        for (int gg = 0; gg < 2; ++gg) {
+          const uint32_t qp = gg ? kq.y : kq.x;
+          const float kz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
+          const float ks = __half2float(__ushort_as_half((unsigned short)(qp >> 16)));
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const int chunk = half * 8 + gg * 4 + c8;          // 8-channel chunk 0..15
+            uint4 craw;
+            if (CS) craw = *reinterpret_cast<const uint4*>(Cs + cswz(idx, chunk));
+            else craw = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)idx * kD + 8 * chunk));
+            const uint32_t cw[4] = {craw.x, craw.y, craw.z, craw.w};
+            const uint32_t bits = (kw[gg * 2 + (c8 >> 1)] >> (16 * (c8 & 1))) & 0xffffu;
+            uint32_t ph[4], pl[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              float kv[2];
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int e = 2 * e2 + u;
+                const float code = (float)((bits >> (2 * e)) & 3u);
+                const float cval = __uint_as_float(u ? (cw[e2] & 0xffff0000u) : (cw[e2] << 16));
+                kv[u] = cval + fmaf(code, ks, kz);
+              }
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(kv[0], kv[1]);
+              const float2 hf = __bfloat1622float2(hb);
+              const __nv_bfloat162 lb = __floats2bfloat162_rn(kv[0] - hf.x, kv[1] - hf.y);
+              ph[e2] = *reinterpret_cast<const uint32_t*>(&hb);
+              pl[e2] = *reinterpret_cast<const uint32_t*>(&lb);
+            }
+            const int off = sw128_off(key, chunk);
+            *reinterpret_cast<uint4*>(Khi + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+            *reinterpret_cast<uint4*>(Klo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+          }
+        }
+        if constexpr (RP > 0) {
+          if (half == 0) {
+            const __half* esrc = reinterpret_cast<const __half*>(tb + a.off.e) + key * a.r;
+#pragma unroll
+            for (int j = 0; j < RP / 8; ++j) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int m0 = 8 * j + 2 * e;
+                const __half e0 = m0 < a.r ? esrc[m0] : __float2half_rn(0.f);
+                const __half e1 = m0 + 1 < a.r ? esrc[m0 + 1] : __float2half_rn(0.f);
+                const __half2 ee = __halves2half2(e0, e1);
+                w[e] = *reinterpret_cast<const uint32_t*>(&ee);
+              }
+              *reinterpret_cast<uint4*>(Es + ((key >> 3) * (RP / 8) + j) * 128 + (key & 7) * 16) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+        }
+      }
+      fence_async_smem();
+      bar_arrive(k_ready);
+      // ---- v_hat^T ----
+      if (t > 0) {
+        if (!bar_wait(pv_done, (uint32_t)((t - 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+      }
+      {
+        const int kb = p & 15, cb = p >> 4;          // keys 8kb.., channels 8cb..
+        const int g = cb >> 2;
+        float vv[8][8];                              // [key][channel]
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int key = 8 * kb + kk;
+          const uint32_t bits = *reinterpret_cast<const uint16_t*>(tb + a.off.vcode + key * 32 + 2 * cb);
+          const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.vqp + (key * G + g) * 4);
+          const float vz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
+          const float vs = __half2float(__ushort_as_half((unsigned short)(qp >> 16)));
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vv[kk][e] = fmaf((float)((bits >> (2 * e)) & 3u), vs, vz);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int dch = 8 * cb + e;
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const __half2 hh = __floats2half2_rn(vv[2 * q][e], vv[2 * q + 1][e]);
+            w[q] = *reinterpret_cast<const uint32_t*>(&hh);
+          }
+          *reinterpret_cast<uint4*>(Vt + sw128_off(dch, kb)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_async_smem();
+      bar_arrive(v_ready);
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = lane == 0;
+    bool ok = true;
+    const uint32_t qa = su32(Qs), kh = su32(Khi), kl = su32(Klo), vt = su32(Vt);
+    const uint32_t ea = su32(Es), za = su32(Zh), zl = su32(Zl);
+    constexpr uint32_t kSbo = (RP / 8) * 128;
+    for (int64_t t = 0; t <= nt && ok; ++t) {
+      if (t < nt) {
+        const int b = (int)(t & 1);
+        if (!bar_wait(k_ready, (uint32_t)(t & 1), &abort_sh, a.status)) { ok = false; break; }
+        if (t >= 2 && !bar_wait(&s_free[b], (uint32_t)(((t >> 1) - 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+        fence_after();
+        if (leader) {
+          const uint32_t d = tmem + kColS0 + 128u * b;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+            mma_ss(d, desc_sw128(qa + ko), desc_sw128(kh + ko), kIdescQK, j > 0);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+            mma_ss(d, desc_sw128(qa + ko), desc_sw128(kl + ko), kIdescQK, 1);
+          }
+          if constexpr (RP > 0) {
+#pragma unroll
+            for (int kk = 0; kk < RP / 16; ++kk) {
+              mma_ss(d, desc_none(za + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
+              mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
+            }
+          }
+          commit(&s_done[b]);
+        }
+        __syncwarp();
+      }
+      if (t >= 1) {
+        const int64_t u = t - 1;
+        if (!bar_wait(p_ready, (uint32_t)(u & 1), &abort_sh, a.status)) { ok = false; break; }
+        if (!bar_wait(v_ready, (uint32_t)(u & 1), &abort_sh, a.status)) { ok = false; break; }
+        fence_after();
+        if (leader) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+            mma_ts(tmem + kColO, tmem + kColP + 8 * j, desc_sw128(vt + ko), kIdescF16, (u > 0 || j > 0) ? 1u : 0u);
+          }
+          commit(pv_done);
+        }
+        __syncwarp();
+      }
+    }
+    // wait for the last PV before the TMEM can be released (bounded)
+    if (ok && nt > 0) bar_wait(pv_done, (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+  }
+
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == 12) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
+size_t tc_smem(const qwm_ctx* c, int RP, bool cs) {
+  return 1024 + 4 * 32768 + 3 * (size_t)128 * RP * 2 + (cs ? (size_t)c->cfg.n_centroids * 256 : 0);
+}
+
+template <int RP, bool CS>
+cudaError_t launch_rp(const qwm_ctx* c, const TcArgs& a, int64_t M, cudaStream_t st) {
+  const size_t smem = tc_smem(c, RP, CS);
+  auto kern = attend_tc_kernel<RP, CS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((M + 127) / 128), (unsigned)c->cfg.heads);
+  kern<<<grid, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool attend_tc_supported(const qwm_ctx* c) {
+  return c->cfg.dtype == QWM_BF16 && c->cfg.head_dim == kD && c->cfg.rank <= 32;
+}
+
+cudaError_t launch_attend_tc(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                             cudaStream_t st) {
+  TcArgs a;
+  a.Q = (const __nv_bfloat16*)q;
+  a.O = (__nv_bfloat16*)out;
+  a.M = M;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.cache = c->cache;
+  a.max_tiles = c->lay.max_tiles;
+  a.off = tile_offsets(c->lay);
+  a.n_tiles = c->n_tiles;
+  a.tiles = c->tiles;
+  a.cent = (const __nv_bfloat16*)c->centroids;
+  a.nC = c->cfg.n_centroids;
+  a.basis = c->basis;
+  a.H = c->cfg.heads;
+  a.r = c->cfg.rank;
+  a.ib = c->ib;
+  a.status = c->status;
+  const int RP = a.r == 0 ? 0 : (a.r <= 16 ? 16 : 32);
+  const bool cs = c->cfg.n_centroids <= 256;
+  if (RP == 0) return cs ? launch_rp<0, true>(c, a, M, st) : launch_rp<0, false>(c, a, M, st);
+  if (RP == 16) return cs ? launch_rp<16, true>(c, a, M, st) : launch_rp<16, false>(c, a, M, st);
+  return cs ? launch_rp<32, true>(c, a, M, st) : launch_rp<32, false>(c, a, M, st);
+}
+
+}  // namespace qwm

@@ -9,8 +9,8 @@
 //    fixed order), one CTA per (head, row block).
 // 2. eig_kernel, one CTA per head: sums the partials in a fixed order, writes
 //    s_c = G_cc / n_h, then finds the top-r eigenvectors of G by block
-//    subspace iteration (start block = unit vectors of the largest diagonal
-//    entries, modified Gram-Schmidt twice per step) with a two-pass
+//    subspace iteration on G^2 (start block = unit vectors of the largest
+//    diagonal entries, modified Gram-Schmidt twice per step) with a two-pass
 //    Rayleigh-Ritz (parallel cyclic Jacobi on the projected matrix, then once
 //    more on the re-orthonormalised Ritz vectors, which restores
 //    orthogonality to float32 precision).  When r + oversample exceeds 64 the
@@ -25,13 +25,17 @@
 namespace qwm {
 namespace {
 
-constexpr int kRowsPerSplit = 512;
+constexpr int kRowsPerSplit = 128;
+constexpr int kMaxSplits = 32;
 constexpr int kEigThreads = 256;
-constexpr int kCheckEvery = 4;
+constexpr int kCheckEvery = 2;       // A^2 iterations between Rayleigh-Ritz checks
 constexpr float kResidualTol = 2e-6f;
 constexpr float kShift = 9.5367431640625e-07f;   // 2^-20 of the mean eigenvalue
 
-int splits_for(int64_t n_h) { return (int)((n_h + kRowsPerSplit - 1) / kRowsPerSplit); }
+int splits_for(int64_t n_h) {
+  const int s = (int)((n_h + kRowsPerSplit - 1) / kRowsPerSplit);
+  return s < kMaxSplits ? s : kMaxSplits;
+}
 
 int eig_cols(const qwm_config& c) {
   int m = c.rank + c.oversample;
@@ -42,7 +46,8 @@ int eig_cols(const qwm_config& c) {
 // ------------------------------------------------------------------ Gram
 template <int D, typename T>
 __global__ void __launch_bounds__(256) gram_kernel(const T* __restrict__ Q, int64_t n_h,
-                                                   float* __restrict__ part, int splits) {
+                                                   float* __restrict__ part, int splits,
+                                                   int64_t rows_per_split) {
   constexpr int TI = D / 16;           // each thread owns a TI x TI block of G
   __shared__ float qs[32][D];
   const int h = blockIdx.x, sp = blockIdx.y;
@@ -52,8 +57,8 @@ __global__ void __launch_bounds__(256) gram_kernel(const T* __restrict__ Q, int6
   for (int i = 0; i < TI; ++i)
 #pragma unroll
     for (int j = 0; j < TI; ++j) acc[i][j] = 0.f;
-  const int64_t r0 = (int64_t)sp * kRowsPerSplit;
-  const int64_t r1 = min(n_h, r0 + kRowsPerSplit);
+  const int64_t r0 = (int64_t)sp * rows_per_split;
+  const int64_t r1 = min(n_h, r0 + rows_per_split);
   const T* qh = Q + (int64_t)h * n_h * D;
   for (int64_t rb = r0; rb < r1; rb += 32) {
     const int nr = (int)min((int64_t)32, r1 - rb);
@@ -108,7 +113,8 @@ __device__ __forceinline__ void rr_pair(int ne, int k, int a, int* p, int* q) {
 // float32), rotations accumulated into V (caller initialises it).  The
 // rotation of pair (p, q) uses t = -sign(th)/(|th| + sqrt(th^2+1)),
 // th = (A_pp - A_qq)/(2 A_pq), c = 1/sqrt(1+t^2), s = t c, which zeroes
-// A'_pq; it is skipped when |A_pq| <= 2^-23 sqrt(|A_pp A_qq|).  Each step
+// A'_pq; it is skipped when |A_pq| <= 2^-20 sqrt(|A_pp A_qq|) (float32
+// rounding keeps smaller off-diagonals alive forever).  Each step
 // updates every 2x2 block (pair a rows, pair b columns) in place.  Returns
 // the sweeps used (at most max_sweeps).
 __device__ int jacobi(float* A, int lda, float* V, int ldv, int n, int max_sweeps, float* rot,
@@ -125,7 +131,7 @@ __device__ int jacobi(float* A, int lda, float* V, int ldv, int n, int max_sweep
         float c = 1.f, s = 0.f;
         if (p < n && q < n) {
           const float app = A[p * lda + p], aqq = A[q * lda + q], apq = A[p * lda + q];
-          if (apq != 0.f && fabsf(apq) > 1.1920929e-07f * sqrtf(fabsf(app * aqq))) {
+          if (apq != 0.f && fabsf(apq) > 9.5367431640625e-07f * sqrtf(fabsf(app * aqq))) {
             const float th = (app - aqq) / (2.f * apq);
             const float t = (th >= 0.f ? -1.f : 1.f) / (fabsf(th) + sqrtf(th * th + 1.f));
             c = 1.f / sqrtf(t * t + 1.f);
@@ -174,8 +180,75 @@ __device__ int jacobi(float* A, int lda, float* V, int ldv, int n, int max_sweep
   return sweep + 1;
 }
 
-// Modified Gram-Schmidt, twice, on the m columns of X (d rows, leading dim ldx).
-__device__ void mgs2(float* X, int ldx, int d, int m, float* tmp) {
+// Modified Gram-Schmidt, twice, on the m <= 64 columns of X (d rows, leading
+// dim ldx).  Column k lives in the registers of warp k % 8 (d/32 values per
+// lane); the owner of column j normalises it and publishes it through a
+// double-buffered shared row, then every warp projects its later columns
+// against it: one block barrier per column and pass.
+template <int D>
+__device__ void mgs2(float* X, int ldx, int m, float* colbuf /* [2][D] */) {
+  constexpr int J = D / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float v[8][J];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int k = warp + 8 * c;
+#pragma unroll
+    for (int j = 0; j < J; ++j) v[c][j] = k < m ? X[(lane + 32 * j) * ldx + k] : 0.f;
+  }
+  int step = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int j = 0; j < m; ++j, ++step) {
+      float* cb = colbuf + (step & 1) * D;
+      if (warp == (j & 7)) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          if (c == (j >> 3)) {
+            float s2 = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < J; ++jj) s2 = fmaf(v[c][jj], v[c][jj], s2);
+            s2 = warp_sum(s2);
+            const float inv = s2 > 0.f ? 1.f / sqrtf(s2) : 0.f;
+#pragma unroll
+            for (int jj = 0; jj < J; ++jj) {
+              v[c][jj] *= inv;
+              cb[lane + 32 * jj] = v[c][jj];
+            }
+          }
+        }
+      }
+      __syncthreads();
+      float u[J];
+#pragma unroll
+      for (int jj = 0; jj < J; ++jj) u[jj] = cb[lane + 32 * jj];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int k = warp + 8 * c;
+        if (k > j && k < m) {
+          float dt = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < J; ++jj) dt = fmaf(u[jj], v[c][jj], dt);
+          dt = warp_sum(dt);
+#pragma unroll
+          for (int jj = 0; jj < J; ++jj) v[c][jj] = fmaf(-dt, u[jj], v[c][jj]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int k = warp + 8 * c;
+    if (k < m) {
+#pragma unroll
+      for (int j = 0; j < J; ++j) X[(lane + 32 * j) * ldx + k] = v[c][j];
+    }
+  }
+  __syncthreads();
+}
+
+// Full-matrix Modified Gram-Schmidt, twice (the m = d path), with block
+// barriers; used once per calibration.
+__device__ void mgs2_block(float* X, int ldx, int d, int m, float* tmp) {
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
   for (int pass = 0; pass < 2; ++pass) {
     for (int j = 0; j < m; ++j) {
@@ -200,14 +273,36 @@ __device__ void mgs2(float* X, int ldx, int d, int m, float* tmp) {
   }
 }
 
-// W (d x m) = A (d x d) X (d x m)
+// W (d x m) = A (d x d) X (d x m).  A thread computes rows ri, ri+32,
+// ri+64, ri+96 (those below d) of 4 consecutive columns: the 32 lanes of a
+// warp read 32 different rows of A (conflict-free with its odd leading dim)
+// and the same entries of X (broadcast).
 __device__ void matmul_ax(const float* A, int lda, const float* X, int ldx, float* W, int ldw, int d,
                           int m) {
-  for (int idx = threadIdx.x; idx < d * m; idx += blockDim.x) {
-    const int i = idx % d, k = idx / d;
-    float s = 0.f;
-    for (int l = 0; l < d; ++l) s = fmaf(A[i * lda + l], X[l * ldx + k], s);
-    W[i * ldw + k] = s;
+  const int cgroups = (m + 3) / 4;
+  for (int tile = threadIdx.x; tile < 32 * cgroups; tile += blockDim.x) {
+    const int ri = tile % 32, cg = tile / 32;
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+    for (int l = 0; l < d; ++l) {
+      float xa[4], ar[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) xa[b] = (4 * cg + b < m) ? X[l * ldx + 4 * cg + b] : 0.f;
+#pragma unroll
+      for (int a = 0; a < 4; ++a) ar[a] = (ri + 32 * a < d) ? A[(ri + 32 * a) * lda + l] : 0.f;
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(ar[a], xa[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        if (ri + 32 * a < d && 4 * cg + b < m) W[(ri + 32 * a) * ldw + 4 * cg + b] = acc[a][b];
   }
   __syncthreads();
 }
@@ -268,10 +363,11 @@ __device__ void set_identity(float* V, int ldv, int m) {
   __syncthreads();
 }
 
-// Buffers of the eigen-solver for one head, as float offsets.
+// Buffers of the eigen-solver for one head, as float offsets.  A2 = A^2 is
+// kept only on the subspace path (m < d).
 struct EigLayout {
   int ldg, ldm, m;
-  size_t g, x, w, h, v, floats;
+  size_t g, g2, x, w, h, v, floats;
 };
 
 __host__ __device__ inline EigLayout eig_layout(int d, int m) {
@@ -280,7 +376,8 @@ __host__ __device__ inline EigLayout eig_layout(int d, int m) {
   L.ldg = d + 1;
   L.ldm = m + 1;
   L.g = 0;
-  L.x = L.g + (size_t)d * L.ldg;
+  L.g2 = L.g + (size_t)d * L.ldg;
+  L.x = L.g2 + (m < d ? (size_t)d * L.ldg : 0);
   L.w = L.x + (size_t)d * L.ldm;
   L.h = L.w + (size_t)d * L.ldm;
   L.v = L.h + (size_t)m * L.ldm;
@@ -306,6 +403,7 @@ eig_kernel(const float* __restrict__ part, int splits, int64_t n_h, int r, int m
   const EigLayout L = eig_layout(D, m);
   float* base = use_smem ? smem : gws + (size_t)h * L.floats;
   float* A = base + L.g;
+  float* A2 = base + L.g2;
   float* X = base + L.x;
   float* W = base + L.w;
   float* Hm = base + L.h;
@@ -377,28 +475,30 @@ eig_kernel(const float* __restrict__ part, int splits, int64_t n_h, int r, int m
     __syncthreads();
   }
 
+  if (!full) matmul_ax(A, L.ldg, A, L.ldg, A2, L.ldg, D, D);   // iterate on A^2
   while (true) {
     if (!full) {
       for (int t = 0; t < kCheckEvery && iters < max_iter; ++t, ++iters) {
-        matmul_ax(A, L.ldg, X, L.ldm, W, L.ldm, D, m);
+        matmul_ax(A2, L.ldg, X, L.ldm, W, L.ldm, D, m);
         for (int idx = tid; idx < D * m; idx += blockDim.x)
           X[(idx / m) * L.ldm + idx % m] = W[(idx / m) * L.ldm + idx % m];
         __syncthreads();
-        mgs2(X, L.ldm, D, m, tmp);
+        mgs2<D>(X, L.ldm, m, wbuf);
       }
-      // Rayleigh-Ritz, first pass
+      // Rayleigh-Ritz on A, first pass
       matmul_ax(A, L.ldg, X, L.ldm, W, L.ldm, D, m);
       project(X, L.ldm, W, L.ldm, Hm, L.ldm, D, m);
       set_identity(V, L.ldm, m);
-      jacobi(Hm, L.ldm, V, L.ldm, m, 16, rot, prs);
+      jacobi(Hm, L.ldm, V, L.ldm, m, 12, rot, prs);
       rotate_sorted(X, L.ldm, D, m, V, L.ldm, Hm, L.ldm, theta, order, wbuf);
     }
     // second pass on the re-orthonormalised Ritz vectors
-    mgs2(X, L.ldm, D, m, tmp);
+    if (full) mgs2_block(X, L.ldm, D, m, tmp);
+    else mgs2<D>(X, L.ldm, m, wbuf);
     matmul_ax(A, L.ldg, X, L.ldm, W, L.ldm, D, m);
     project(X, L.ldm, W, L.ldm, Hm, L.ldm, D, m);
     set_identity(V, L.ldm, m);
-    jacobi(Hm, L.ldm, V, L.ldm, m, 6, rot, prs);
+    jacobi(Hm, L.ldm, V, L.ldm, m, 4, rot, prs);
     rotate_sorted(X, L.ldm, D, m, V, L.ldm, Hm, L.ldm, theta, order, wbuf);
     rotate_sorted(W, L.ldm, D, m, V, L.ldm, Hm, L.ldm, theta, order, wbuf);
     // residuals of the leading r Ritz pairs
@@ -478,14 +578,15 @@ size_t gram_workspace_bytes(const qwm_config& c) {
 
 cudaError_t launch_gram(const qwm_ctx* c, const void* q, int64_t n_h, cudaStream_t st) {
   const int sp = splits_for(n_h);
+  const int64_t rps = (n_h + sp - 1) / sp;
   dim3 grid(c->cfg.heads, sp);
   float* part = (float*)c->ws;
   if (c->cfg.head_dim == 128) {
-    if (c->cfg.dtype == QWM_BF16) gram_kernel<128, __nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)q, n_h, part, sp);
-    else gram_kernel<128, float><<<grid, 256, 0, st>>>((const float*)q, n_h, part, sp);
+    if (c->cfg.dtype == QWM_BF16) gram_kernel<128, __nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)q, n_h, part, sp, rps);
+    else gram_kernel<128, float><<<grid, 256, 0, st>>>((const float*)q, n_h, part, sp, rps);
   } else {
-    if (c->cfg.dtype == QWM_BF16) gram_kernel<64, __nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)q, n_h, part, sp);
-    else gram_kernel<64, float><<<grid, 256, 0, st>>>((const float*)q, n_h, part, sp);
+    if (c->cfg.dtype == QWM_BF16) gram_kernel<64, __nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)q, n_h, part, sp, rps);
+    else gram_kernel<64, float><<<grid, 256, 0, st>>>((const float*)q, n_h, part, sp, rps);
   }
   return cudaGetLastError();
 }
@@ -497,7 +598,7 @@ cudaError_t launch_eig(const qwm_ctx* c, int64_t n_h, int32_t version, cudaStrea
   const size_t part_bytes = (size_t)H * splits_for(c->cfg.max_hist) * D * D * 4;
   float* gws = (float*)(c->ws + ((part_bytes + 255) & ~size_t(255)));
   const size_t bytes = L.floats * 4;
-  const int use_smem = bytes <= 160 * 1024;
+  const int use_smem = bytes <= 210 * 1024;
   const size_t smem = use_smem ? bytes : 0;
   float* U = c->basis + (size_t)version * H * (r > 0 ? r : 1) * D;   // version = basis slot
   const int sp = splits_for(n_h);

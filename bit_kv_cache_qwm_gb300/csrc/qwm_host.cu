@@ -250,9 +250,10 @@ extern "C" qwm_status qwm_attend(qwm_ctx* x, const void* d_q, int64_t M, float s
   if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)x->cfg.head_dim);
   int k = qwm_resolved_attend_kernel(x);
   if (k == 2 && !attend_mma_supported(x)) return QWM_ERR_UNSUPPORTED;
-  if (k == 3) return QWM_ERR_UNSUPPORTED;
-  cudaError_t e = k == 2 ? launch_attend_mma(x, d_q, M, scale, d_out, S(stream))
-                         : launch_attend_simt(x, d_q, M, scale, d_out, S(stream));
+  if (k == 3 && !attend_tc_supported(x)) return QWM_ERR_UNSUPPORTED;
+  cudaError_t e = k == 3   ? launch_attend_tc(x, d_q, M, scale, d_out, S(stream))
+                  : k == 2 ? launch_attend_mma(x, d_q, M, scale, d_out, S(stream))
+                           : launch_attend_simt(x, d_q, M, scale, d_out, S(stream));
   return cuda_status(e);
 }
 

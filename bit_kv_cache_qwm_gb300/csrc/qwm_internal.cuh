@@ -68,6 +68,9 @@ cudaError_t launch_attend_simt(const qwm_ctx* c, const void* q, int64_t M, float
 cudaError_t launch_attend_mma(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
                               cudaStream_t st);
 bool attend_mma_supported(const qwm_ctx* c);
+cudaError_t launch_attend_tc(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                             cudaStream_t st);
+bool attend_tc_supported(const qwm_ctx* c);
 size_t gram_workspace_bytes(const qwm_config& cfg);
 
 // ---- device helpers ----

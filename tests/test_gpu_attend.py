@@ -117,7 +117,7 @@ def test_full_rank_compensation_on_gpu(qwm, kernel):
     assert np.abs(got - want).max() <= 1e-5 * vmax
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_attend_bf16_sampled_rows(qwm, kernel):
     """12 heads over 3 appends; the oracle checks every row of heads 0 and 9."""
     name = "bf16-h12-n32760"
@@ -129,7 +129,7 @@ def test_attend_bf16_sampled_rows(qwm, kernel):
     assert np.abs(got[[0, 9]] - want).max() <= 1e-2 * vmax
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 @pytest.mark.parametrize("name,C,r", [("bf16-h12-n32760", 256, 16), ("bf16-h24-append-sweep", 1024, 32),
                                       ("bf16-h24-append-sweep", 64, 8), ("bf16-h24-append-sweep", 256, 0),
                                       ("bf16-h40-n98280-outlier", 256, 16)])
