@@ -14,8 +14,9 @@
 // negated, in shared memory as float32, 64 KiB at a time; every lane of a
 // quarter-warp reads the same address, so the loads are broadcasts.  The
 // score of a centroid is formed exactly as the decision definition states:
-// f32 residual, exact max/min, R*R, w*R^2, fixed tree sum, strict < so the
-// lowest index wins a tie.
+// f32 residual, exact max/min (their evaluation order does not matter), R*R,
+// w*R^2, fixed tree sum, strict < in ascending index order so the lowest
+// index wins a tie.
 #include "qwm_internal.cuh"
 
 namespace qwm {
@@ -148,41 +149,54 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
     __syncthreads();
     for (int i = threadIdx.x; i < cn * D; i += NT) cs[i] = -load_elem(ch + (int64_t)c0 * D, i);
     __syncthreads();
+    // two centroids per step, each with even/odd partial max/min: eight
+    // independent dependency chains per thread
 #pragma unroll 1
-    for (int j = 0; j < cn; ++j) {
-      const float4* cp = reinterpret_cast<const float4*>(cs + j * D + gi * kGroup);
-      float mx, mn;
-      {
-        const float4 a = cp[0];
-        const float2 r0 = __fadd2_rn(make_float2(kx[0], kx[1]), make_float2(a.x, a.y));
-        const float2 r1 = __fadd2_rn(make_float2(kx[2], kx[3]), make_float2(a.z, a.w));
-        mx = max3(r0.x, r0.y, r1.x);
-        mn = min3(r0.x, r0.y, r1.x);
-        mx = fmaxf(mx, r1.y);
-        mn = fminf(mn, r1.y);
-      }
+    for (int j = 0; j < cn; j += 2) {
+      const bool two = j + 1 < cn;
+      const float4* ca = reinterpret_cast<const float4*>(cs + j * D + gi * kGroup);
+      const float4* cb = reinterpret_cast<const float4*>(cs + (two ? j + 1 : j) * D + gi * kGroup);
+      float ax0 = -INFINITY, ax1 = -INFINITY, an0 = INFINITY, an1 = INFINITY;
+      float bx0 = -INFINITY, bx1 = -INFINITY, bn0 = INFINITY, bn1 = INFINITY;
 #pragma unroll
-      for (int q = 1; q < 8; ++q) {
-        const float4 a = cp[q];
-        const float2 r0 = __fadd2_rn(make_float2(kx[4 * q], kx[4 * q + 1]), make_float2(a.x, a.y));
-        const float2 r1 = __fadd2_rn(make_float2(kx[4 * q + 2], kx[4 * q + 3]), make_float2(a.z, a.w));
-        mx = max3(mx, r0.x, r0.y);
-        mn = min3(mn, r0.x, r0.y);
-        mx = max3(mx, r1.x, r1.y);
-        mn = min3(mn, r1.x, r1.y);
+      for (int q = 0; q < 8; q += 2) {
+        const float4 a0 = ca[q], a1 = ca[q + 1], b0 = cb[q], b1 = cb[q + 1];
+        const float2 k01 = make_float2(kx[4 * q], kx[4 * q + 1]), k23 = make_float2(kx[4 * q + 2], kx[4 * q + 3]);
+        const float2 k45 = make_float2(kx[4 * q + 4], kx[4 * q + 5]), k67 = make_float2(kx[4 * q + 6], kx[4 * q + 7]);
+        const float2 ra0 = __fadd2_rn(k01, make_float2(a0.x, a0.y)), ra1 = __fadd2_rn(k23, make_float2(a0.z, a0.w));
+        const float2 ra2 = __fadd2_rn(k45, make_float2(a1.x, a1.y)), ra3 = __fadd2_rn(k67, make_float2(a1.z, a1.w));
+        const float2 rb0 = __fadd2_rn(k01, make_float2(b0.x, b0.y)), rb1 = __fadd2_rn(k23, make_float2(b0.z, b0.w));
+        const float2 rb2 = __fadd2_rn(k45, make_float2(b1.x, b1.y)), rb3 = __fadd2_rn(k67, make_float2(b1.z, b1.w));
+        ax0 = max3(ax0, ra0.x, ra0.y); an0 = min3(an0, ra0.x, ra0.y);
+        ax1 = max3(ax1, ra1.x, ra1.y); an1 = min3(an1, ra1.x, ra1.y);
+        bx0 = max3(bx0, rb0.x, rb0.y); bn0 = min3(bn0, rb0.x, rb0.y);
+        bx1 = max3(bx1, rb1.x, rb1.y); bn1 = min3(bn1, rb1.x, rb1.y);
+        ax0 = max3(ax0, ra2.x, ra2.y); an0 = min3(an0, ra2.x, ra2.y);
+        ax1 = max3(ax1, ra3.x, ra3.y); an1 = min3(an1, ra3.x, ra3.y);
+        bx0 = max3(bx0, rb2.x, rb2.y); bn0 = min3(bn0, rb2.x, rb2.y);
+        bx1 = max3(bx1, rb3.x, rb3.y); bn1 = min3(bn1, rb3.x, rb3.y);
       }
-      const float R = __fsub_rn(mx, mn);
-      const float tg = __fmul_rn(wg, __fmul_rn(R, R));
-      float S;
+      const float Ra = __fsub_rn(fmaxf(ax0, ax1), fminf(an0, an1));
+      const float Rb = __fsub_rn(fmaxf(bx0, bx1), fminf(bn0, bn1));
+      const float ta = __fmul_rn(wg, __fmul_rn(Ra, Ra));
+      const float tb = __fmul_rn(wg, __fmul_rn(Rb, Rb));
+      float Sa, Sb;
       if (G == 4) {
-        const float u = __fadd_rn(tg, __shfl_xor_sync(kFull, tg, TPW));
-        S = __fadd_rn(u, __shfl_xor_sync(kFull, u, 2 * TPW));
+        const float ua = __fadd_rn(ta, __shfl_xor_sync(kFull, ta, TPW));
+        const float ub = __fadd_rn(tb, __shfl_xor_sync(kFull, tb, TPW));
+        Sa = __fadd_rn(ua, __shfl_xor_sync(kFull, ua, 2 * TPW));
+        Sb = __fadd_rn(ub, __shfl_xor_sync(kFull, ub, 2 * TPW));
       } else {
-        S = __fadd_rn(tg, __shfl_xor_sync(kFull, tg, TPW));
+        Sa = __fadd_rn(ta, __shfl_xor_sync(kFull, ta, TPW));
+        Sb = __fadd_rn(tb, __shfl_xor_sync(kFull, tb, TPW));
       }
-      if (S < best) {
-        best = S;
+      if (Sa < best) {
+        best = Sa;
         bj = c0 + j;
+      }
+      if (two && Sb < best) {
+        best = Sb;
+        bj = c0 + j + 1;
       }
     }
   }

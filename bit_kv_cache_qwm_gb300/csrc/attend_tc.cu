@@ -137,6 +137,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 __device__ __forceinline__ void prod_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kProdThreads) : "memory"); }
+// AND of a predicate over the 256 producer threads (named barrier 1): every
+// producer takes the same branch after a bounded wait, so none is left behind
+// at a later producer barrier.
+__device__ __forceinline__ bool prod_all(bool v) {
+  uint32_t r;
+  asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, %2, p;\n"
+               "selp.u32 %0, 1, 0, q;\n}"
+               : "=r"(r) : "r"((uint32_t)v), "n"(kProdThreads) : "memory");
+  return r != 0;
+}
+// warp-uniform result of a bounded wait: tcgen05.ld/st are warp-collective
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
 // byte offset of (row, k) in a [128 rows][128 k] 16-bit tile stored as two
 // SW128 K-major atoms of 64 k each (chunk = 8 elements)
@@ -223,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     for (int64_t t = 0; t < nt && ok; ++t) {
       const int b = (int)(t & 1);
       const int nv = a.tiles[t].y;
-      if (!bar_wait(&s_done[b], (uint32_t)((t >> 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+      if (!warp_all(bar_wait(&s_done[b], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       fence_after();
       const uint32_t sbase = tmem + lane_base + kColS0 + 128u * b;
       float mx = -INFINITY;
@@ -237,24 +249,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       }
       const float mnew = fmaxf(m_run, mx * c2);
       if (t > 0) {
-        if (!bar_wait(pv_done, (uint32_t)((t - 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+        if (!warp_all(bar_wait(pv_done, (uint32_t)((t - 1) & 1), &abort_sh, a.status))) { ok = false; break; }
         fence_after();
       }
-      if (mnew > m_run + 8.f) {
-        if (t > 0) {
-          const float corr = ex2(m_run - mnew);
-          for (int cb = 0; cb < 4; ++cb) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kColO + 32 * cb, v);
-            tmem_wait_ld();
+      // lazy rescale: only rows whose maximum grew by more than 2^8 change,
+      // but the TMEM traffic is issued by the whole warp (factor 1 elsewhere)
+      const bool need = mnew > m_run + 8.f;
+      if (t > 0 && __any_sync(0xffffffffu, need)) {
+        const float corr = need ? ex2(m_run - mnew) : 1.f;
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kColO + 32 * cb, v);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-            tmem_st32(tmem + lane_base + kColO + 32 * cb, v);
-          }
-          l_run *= corr;
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+          tmem_st32(tmem + lane_base + kColO + 32 * cb, v);
         }
-        m_run = mnew;
+        l_run *= corr;
       }
+      if (need) m_run = mnew;
       float psum = 0.f;
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t v[32], pk[16];
@@ -278,27 +291,29 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       bar_arrive(&s_free[b]);
       bar_arrive(p_ready);
     }
-    // epilogue
-    if (ok && nt > 0) ok = bar_wait(pv_done, (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+    // epilogue: every lane loads (warp-collective), valid rows store
+    if (ok && nt > 0) ok = warp_all(bar_wait(pv_done, (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
     fence_after();
     const int64_t row = row0 + tid;
-    if (ok && row < a.M) {
+    if (ok) {
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       __nv_bfloat16* dst = a.O + ((int64_t)h * a.M + row) * kD;
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kColO + 32 * cb, v);
         tmem_wait_ld();
+        if (row < a.M) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t w[4];
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __nv_bfloat162 bb = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]) * inv,
-                                                            __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
-            w[e] = *reinterpret_cast<const uint32_t*>(&bb);
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 bb = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * e]) * inv,
+                                                              __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * cb + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          *reinterpret_cast<uint4*>(dst + 32 * cb + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       const uint8_t* tb = tiles_h + t * a.off.bytes;
       const int slot = a.tiles[t].x;
       if (t > 0) {
-        if (!bar_wait(&s_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+        if (!prod_all(bar_wait(&s_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       }
       if constexpr (RP > 0) {
         if (slot != cur_slot) {
@@ -443,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       bar_arrive(k_ready);
       // ---- v_hat^T ----
       if (t > 0) {
-        if (!bar_wait(pv_done, (uint32_t)((t - 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+        if (!prod_all(bar_wait(pv_done, (uint32_t)((t - 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       }
       {
         const int kb = p & 15, cb = p >> 4;          // keys 8kb.., channels 8cb..
@@ -484,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     for (int64_t t = 0; t <= nt && ok; ++t) {
       if (t < nt) {
         const int b = (int)(t & 1);
-        if (!bar_wait(k_ready, (uint32_t)(t & 1), &abort_sh, a.status)) { ok = false; break; }
-        if (t >= 2 && !bar_wait(&s_free[b], (uint32_t)(((t >> 1) - 1) & 1), &abort_sh, a.status)) { ok = false; break; }
+        if (!warp_all(bar_wait(k_ready, (uint32_t)(t & 1), &abort_sh, a.status))) { ok = false; break; }
+        if (t >= 2 && !warp_all(bar_wait(&s_free[b], (uint32_t)(((t >> 1) - 1) & 1), &abort_sh, a.status))) { ok = false; break; }
         fence_after();
         if (leader) {
           const uint32_t d = tmem + kColS0 + 128u * b;
@@ -512,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       }
       if (t >= 1) {
         const int64_t u = t - 1;
-        if (!bar_wait(p_ready, (uint32_t)(u & 1), &abort_sh, a.status)) { ok = false; break; }
-        if (!bar_wait(v_ready, (uint32_t)(u & 1), &abort_sh, a.status)) { ok = false; break; }
+        if (!warp_all(bar_wait(p_ready, (uint32_t)(u & 1), &abort_sh, a.status))) { ok = false; break; }
+        if (!warp_all(bar_wait(v_ready, (uint32_t)(u & 1), &abort_sh, a.status))) { ok = false; break; }
         fence_after();
         if (leader) {
 #pragma unroll
