@@ -19,7 +19,6 @@
 // 3. weights_kernel: w_g = s_{32g} + ... + s_{32g+31}, left to right in
 //    float32 (an input of the centroid decision).
 #include <math.h>
-
 #include "qwm_internal.cuh"
 
 namespace qwm {
@@ -626,3 +625,4 @@ cudaError_t launch_group_weights(const qwm_ctx* c, cudaStream_t st) {
 }
 
 }  // namespace qwm
+

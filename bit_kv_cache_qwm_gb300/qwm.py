@@ -51,7 +51,7 @@ class QwmError(RuntimeError):
 
 
 EXPORTS = ["qwm_status_string", "qwm_sizes", "qwm_create", "qwm_destroy", "qwm_set_centroids",
-           "qwm_calibrate", "qwm_set_calibration", "qwm_get_calibration", "qwm_append",
+           "qwm_calibrate", "qwm_kmeans", "qwm_kmeans_workspace_bytes", "qwm_set_calibration", "qwm_get_calibration", "qwm_append",
            "qwm_attend", "qwm_rewind", "qwm_get_status", "qwm_peek_status_bits",
            "qwm_set_attend_kernel", "qwm_resolved_attend_kernel", "qwm_num_tokens", "qwm_num_tiles", "qwm_num_segments",
            "qwm_version"]
@@ -84,11 +84,14 @@ def lib() -> ctypes.CDLL:
         "qwm_get_status": [VP, VP],
         "qwm_peek_status_bits": [VP, P(ctypes.c_uint32), VP],
         "qwm_set_attend_kernel": [VP, I32],
+        "qwm_kmeans": [I32, I32, I32, I32, VP, I64, VP, I32, VP, VP, VP],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    L.qwm_kmeans_workspace_bytes.restype = ctypes.c_size_t
+    L.qwm_kmeans_workspace_bytes.argtypes = [I32, I32, I32, I64]
     for name, rt in [("qwm_resolved_attend_kernel", I32), ("qwm_num_tokens", I64), ("qwm_num_tiles", I64), ("qwm_num_segments", I32),
                      ("qwm_version", I32)]:
         fn = getattr(L, name)
@@ -111,6 +114,25 @@ def _fptr(a: Optional[np.ndarray]):
     if a is None:
         return None
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def qwm_kmeans(keys: torch.Tensor, init_rows: torch.Tensor, n_centroids: int, iters: int = 25) -> torch.Tensor:
+    """Lloyd's k-means on the GPU: keys [H][n][d] (bf16/f32), init_rows [H][C]
+    int32 on the same device.  Returns centroids [H][C][d] in the keys' dtype."""
+    H, n, d = keys.shape
+    dt = QWM_BF16 if keys.dtype == torch.bfloat16 else QWM_F32
+    if not keys.is_contiguous() or keys.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("keys: contiguous bf16 or f32 tensor expected")
+    rows = init_rows.to(device=keys.device, dtype=torch.int32).contiguous()
+    if tuple(rows.shape) != (H, n_centroids):
+        raise ValueError("init_rows: shape [H, C] expected")
+    ws = torch.empty(lib().qwm_kmeans_workspace_bytes(H, d, n_centroids, n) + 256, dtype=torch.uint8,
+                     device=keys.device)
+    out = torch.empty((H, n_centroids, d), dtype=keys.dtype, device=keys.device)
+    _check(lib().qwm_kmeans(H, d, dt, n_centroids, ctypes.c_void_p(keys.data_ptr()), n,
+                            ctypes.c_void_p(rows.data_ptr()), iters, ctypes.c_void_p(out.data_ptr()),
+                            ctypes.c_void_p(ws.data_ptr()), _stream()), "qwm_kmeans")
+    return out
 
 
 def make_config(heads, head_dim, rank, n_centroids, dtype="bf16", max_tokens=4096, max_versions=4,

@@ -175,6 +175,21 @@ qwm_status qwm_get_status(qwm_ctx* ctx, void* stream);
 /* Same as qwm_get_status but returns the raw bits in *bits. */
 qwm_status qwm_peek_status_bits(qwm_ctx* ctx, uint32_t* bits, void* stream);
 
+/* Lloyd's k-means that builds the centroids QSAC assigns keys to ("each Key is
+ * assigned to a clustering center", roboind article, "Step 1").  keys
+ * [H][n][d] (dtype), d_init_rows [H][C] int32 (device; the starting keys,
+ * e.g. the first C entries of a seeded permutation), `iters` iterations:
+ * assignment to the nearest centroid in float32 squared distance (lowest
+ * index on a tie), update to the float64 mean of the assigned keys rounded to
+ * float32, an empty cluster keeps its centroid.  Output [H][C][d] in dtype
+ * (nearest even), ready for qwm_set_centroids.  d_workspace: at least
+ * qwm_kmeans_workspace_bytes(...) bytes, 256-byte aligned, caller-owned.
+ * Asynchronous. */
+size_t qwm_kmeans_workspace_bytes(int32_t heads, int32_t head_dim, int32_t n_centroids, int64_t n);
+qwm_status qwm_kmeans(int32_t heads, int32_t head_dim, int32_t dtype, int32_t n_centroids,
+                      const void* d_keys, int64_t n, const int32_t* d_init_rows, int32_t iters,
+                      void* d_centroids, void* d_workspace, void* stream);
+
 /* Attention kernel choice: 0 = automatic (tensor-core kernel where it
  * applies), 1 = float32 CUDA-core kernel, 2 = bf16 mma.sync kernel,
  * 3 = bf16 tcgen05 kernel. */
