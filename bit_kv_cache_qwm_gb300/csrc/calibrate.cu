@@ -19,6 +19,10 @@
 // 3. weights_kernel: w_g = s_{32g} + ... + s_{32g+31}, left to right in
 //    float32 (an input of the centroid decision).
 #include <math.h>
+#include <string.h>
+
+#include <mutex>
+
 #include "qwm_internal.cuh"
 
 namespace qwm {
@@ -626,3 +630,110 @@ cudaError_t launch_group_weights(const qwm_ctx* c, cudaStream_t st) {
 
 }  // namespace qwm
 
+// ---------------------------------------------------------------------------
+// Calibration without any device allocation.
+//
+// Some callers cannot allocate device memory at all: a plugin whose host
+// application owns every byte of device memory through its own pool, or a code
+// path that must not call cudaMalloc/cudaFree because those calls can
+// synchronise the device.  For them the Gram partial sums of one calibration
+// live in the file-scope array below instead of a caller workspace.  Every GPU
+// that loads this library holds the array (8 MiB) until the process exits.
+// ---------------------------------------------------------------------------
+namespace qwm {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) float g_calib_scratch[kStaticScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+static float* g_scratch_ptr[kMaxDevices];
+static std::mutex g_scratch_mu;
+
+// Device address of the scratch array on the current device, looked up once
+// per device (host code cannot use the symbol itself as a device address).
+cudaError_t static_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_calib_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace qwm
+
+extern "C" qwm_status qwm_calibrate_static(int32_t heads, int32_t head_dim, int32_t rank, int32_t dtype,
+                                           int32_t max_iter, int32_t oversample, const void* d_q_hist,
+                                           int64_t n_h, float* d_s, float* d_U, float* d_lambda,
+                                           float* d_energy, uint32_t* d_status, void* stream) {
+  using namespace qwm;
+  if (heads < 1 || rank < 0 || rank > head_dim || max_iter < 1 || oversample < 0 || n_h < 1)
+    return QWM_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return QWM_ERR_UNSUPPORTED;
+  if (dtype != QWM_F32 && dtype != QWM_BF16) return QWM_ERR_INVALID_ARG;
+  if (!d_q_hist || !d_s || !d_energy || (rank > 0 && (!d_U || !d_lambda))) return QWM_ERR_INVALID_ARG;
+  const size_t D = head_dim, H = heads;
+  qwm_config cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.heads = heads;
+  cfg.head_dim = head_dim;
+  cfg.rank = rank;
+  cfg.oversample = oversample;
+  const int m = eig_cols(cfg);
+  const EigLayout L = eig_layout(head_dim, m);
+  const bool use_smem = L.floats * 4 <= 210 * 1024;
+  // scratch: [64 status/iteration words][spill of the eigen-solver][partials]
+  const size_t cap = kStaticScratchBytes / sizeof(float);
+  const size_t head_words = 64 + H;
+  const size_t spill = use_smem ? 0 : H * L.floats;
+  const size_t per_split = H * D * D;
+  if (head_words + spill + per_split > cap) return QWM_ERR_CAPACITY;   // too many heads for 8 MiB
+  int splits = splits_for(n_h);
+  const int fit = (int)((cap - head_words - spill) / per_split);
+  if (splits > fit) splits = fit;
+  const int64_t rps = (n_h + splits - 1) / splits;
+  float* scratch = nullptr;
+  if (static_scratch(&scratch) != cudaSuccess) return QWM_ERR_CUDA;
+  uint32_t* status_words = reinterpret_cast<uint32_t*>(scratch);
+  int32_t* iters = reinterpret_cast<int32_t*>(scratch + 64);
+  float* gws = scratch + head_words;
+  float* part = gws + spill;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* status = d_status ? d_status : status_words;
+  if (!d_status && cudaMemsetAsync(status_words, 0, 4, st) != cudaSuccess) return QWM_ERR_CUDA;
+  dim3 grid(heads, splits);
+  if (head_dim == 128) {
+    if (dtype == QWM_BF16) gram_kernel<128, __nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)d_q_hist, n_h, part, splits, rps);
+    else gram_kernel<128, float><<<grid, 256, 0, st>>>((const float*)d_q_hist, n_h, part, splits, rps);
+  } else {
+    if (dtype == QWM_BF16) gram_kernel<64, __nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)d_q_hist, n_h, part, splits, rps);
+    else gram_kernel<64, float><<<grid, 256, 0, st>>>((const float*)d_q_hist, n_h, part, splits, rps);
+  }
+  if (cudaGetLastError() != cudaSuccess) return QWM_ERR_CUDA;
+  const size_t smem = use_smem ? L.floats * 4 : 0;
+  float* lam = rank > 0 ? d_lambda : d_energy;   // not written when rank == 0
+  float* U = rank > 0 ? d_U : d_energy;
+  cudaError_t e;
+  if (head_dim == 128) {
+    e = cudaFuncSetAttribute(eig_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      eig_kernel<128><<<heads, kEigThreads, smem, st>>>(part, splits, n_h, rank, m, max_iter, d_s, U, lam,
+                                                         d_energy, iters, status, gws, use_smem ? 1 : 0);
+  } else {
+    e = cudaFuncSetAttribute(eig_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      eig_kernel<64><<<heads, kEigThreads, smem, st>>>(part, splits, n_h, rank, m, max_iter, d_s, U, lam,
+                                                        d_energy, iters, status, gws, use_smem ? 1 : 0);
+  }
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return QWM_ERR_CUDA;
+  return QWM_OK;
+}

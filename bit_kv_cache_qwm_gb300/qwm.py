@@ -51,7 +51,7 @@ class QwmError(RuntimeError):
 
 
 EXPORTS = ["qwm_status_string", "qwm_sizes", "qwm_create", "qwm_destroy", "qwm_set_centroids",
-           "qwm_calibrate", "qwm_kmeans", "qwm_kmeans_workspace_bytes", "qwm_set_calibration", "qwm_get_calibration", "qwm_append",
+           "qwm_calibrate", "qwm_calibrate_static", "qwm_kmeans", "qwm_kmeans_workspace_bytes", "qwm_set_calibration", "qwm_get_calibration", "qwm_append",
            "qwm_attend", "qwm_rewind", "qwm_get_status", "qwm_peek_status_bits",
            "qwm_set_attend_kernel", "qwm_resolved_attend_kernel", "qwm_num_tokens", "qwm_num_tiles", "qwm_num_segments",
            "qwm_version"]
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
         "qwm_get_status": [VP, VP],
         "qwm_peek_status_bits": [VP, P(ctypes.c_uint32), VP],
         "qwm_set_attend_kernel": [VP, I32],
+        "qwm_calibrate_static": [I32, I32, I32, I32, I32, I32, VP, I64, VP, VP, VP, VP, VP, VP],
         "qwm_kmeans": [I32, I32, I32, I32, VP, I64, VP, I32, VP, VP, VP],
     }
     for name, args in sig.items():
@@ -114,6 +115,30 @@ def _fptr(a: Optional[np.ndarray]):
     if a is None:
         return None
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+
+def qwm_calibrate_static(q_hist: torch.Tensor, rank: int, max_iter: int = 64, oversample: int = 16,
+                         out: Optional[dict] = None) -> dict:
+    """Calibration that allocates nothing on the device inside the library
+    (scratch in a fixed 8 MiB array of the library).  Output buffers are taken
+    from `out` when given (torch float32 tensors on q_hist's device), else
+    allocated here by torch, outside the library."""
+    H, n_h, d = q_hist.shape
+    dt = QWM_BF16 if q_hist.dtype == torch.bfloat16 else QWM_F32
+    if not q_hist.is_contiguous() or q_hist.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("q_hist: contiguous bf16 or f32 tensor expected")
+    dev = q_hist.device
+    if out is None:
+        out = {"s": torch.empty(H, d, dtype=torch.float32, device=dev),
+               "U": torch.empty(H, max(rank, 1), d, dtype=torch.float32, device=dev),
+               "lambda": torch.empty(H, max(rank, 1), dtype=torch.float32, device=dev),
+               "energy": torch.empty(H, dtype=torch.float32, device=dev),
+               "status": torch.zeros(1, dtype=torch.int32, device=dev)}
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    _check(lib().qwm_calibrate_static(H, d, rank, dt, max_iter, oversample, P(q_hist), n_h, P(out["s"]),
+                                      P(out["U"]), P(out["lambda"]), P(out["energy"]), P(out["status"]),
+                                      _stream()), "qwm_calibrate_static")
+    return out
 
 
 def qwm_kmeans(keys: torch.Tensor, init_rows: torch.Tensor, n_centroids: int, iters: int = 25) -> torch.Tensor:

@@ -133,6 +133,36 @@ qwm_status qwm_set_centroids(qwm_ctx* ctx, const void* d_centroids, void* stream
  * sets QWM_DEV_NOT_CONVERGED and keeps the best basis found. */
 qwm_status qwm_calibrate(qwm_ctx* ctx, const void* d_q_hist, int64_t n_h, void* stream);
 
+/* Calibration for callers that cannot allocate device memory.  (The QuantWM
+ * pages have no counterpart of this entry point; it only changes where the
+ * scratch lives.)  Some callers cannot call cudaMalloc at all: a plugin whose
+ * host application owns all device memory through its own pool, or a code
+ * path that must not allocate or free because cudaMalloc/cudaFree may
+ * synchronise the device.  This call needs no context and no workspace: it
+ * computes the same sensitivity s [H][d], basis U [H][r][d], eigenvalues
+ * lambda [H][r] and energy [H] as qwm_calibrate (all float32, caller-owned
+ * device buffers; U and lambda may be NULL when rank is 0) from q_hist
+ * [H][n_h][d] (dtype QWM_F32 or QWM_BF16), with the Gram partial sums in one
+ * 8 MiB array compiled into the library, which every GPU that loads the
+ * library keeps until the process exits.
+ *   - Limit: the partial sums of at least one split, H*d*d floats (plus the
+ *     eigen-solver's spill when rank + oversample > 44 at d = 128), must fit in
+ *     8 MiB; larger requests return QWM_ERR_CAPACITY before any launch.  With
+ *     d = 128 that is up to 127 heads.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) once for that device; make that first call before
+ *     any stream capture.  No call allocates or frees memory.
+ *   - All calls share the one array: calls that overlap on the GPU (two
+ *     streams, or two host threads) race and corrupt each other's results;
+ *     order them.  Nothing in the array needs to start at zero except the
+ *     status word, which the call clears itself.
+ *   - d_status (optional, caller-zeroed) receives QWM_DEV_NOT_CONVERGED when
+ *     the eigen-solver hits max_iter.  Asynchronous on `stream`. */
+qwm_status qwm_calibrate_static(int32_t heads, int32_t head_dim, int32_t rank, int32_t dtype,
+                                int32_t max_iter, int32_t oversample, const void* d_q_hist,
+                                int64_t n_h, float* d_s, float* d_U, float* d_lambda,
+                                float* d_energy, uint32_t* d_status, void* stream);
+
 /* Install a calibration computed elsewhere: s [H][d] and U [H][r][d] (host
  * float32).  Opens a new basis version like qwm_calibrate.  Synchronous. */
 qwm_status qwm_set_calibration(qwm_ctx* ctx, const float* h_s, const float* h_U, void* stream);
