@@ -12,7 +12,8 @@
 // (two for d = 64) group threads of a token sit in lanes TPW apart of one warp
 // and combine their partial scores with two shuffles.  Centroids are staged,
 // negated, in shared memory as float32, 64 KiB at a time; every lane of a
-// quarter-warp reads the same address, so the loads are broadcasts.  The
+// quarter-warp reads the same address, so the loads are broadcasts, and the
+// group slices of a row are padded to start 4 banks apart.  The
 // score of a centroid is formed exactly as the decision definition states:
 // f32 residual, exact max/min (their evaluation order does not matter), R*R,
 // w*R^2, fixed tree sum, strict < in ascending index order so the lowest
@@ -118,10 +119,12 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
   constexpr int G = D / kGroup;
   constexpr int NT = kTile * G;
   constexpr int TPW = 32 / G;            // tokens per warp
-  constexpr int CH = 16384 / D;          // centroids staged per pass (64 KiB)
+  constexpr int CH = 16384 / D;          // centroids staged per pass
+  constexpr int GS = kGroup + 4;         // padded group stride: the G group slices of a
+  constexpr int RS = G * GS;             // row start 4 banks apart (conflict-free LDS.128)
   extern __shared__ __align__(16) float smem[];
-  float* cs = smem;                      // [CH][D] negated centroids
-  float* us = smem + CH * D;             // [r][D] PSAC basis rows
+  float* cs = smem;                      // [CH][G][GS] negated centroids
+  float* us = smem + CH * RS;            // [r][D] PSAC basis rows
 
   const int h = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -147,15 +150,16 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
   for (int c0 = 0; c0 < nC; c0 += CH) {
     const int cn = min(CH, nC - c0);
     __syncthreads();
-    for (int i = threadIdx.x; i < cn * D; i += NT) cs[i] = -load_elem(ch + (int64_t)c0 * D, i);
+    for (int i = threadIdx.x; i < cn * D; i += NT)
+      cs[(i / D) * RS + ((i % D) / kGroup) * GS + (i % kGroup)] = -load_elem(ch + (int64_t)c0 * D, i);
     __syncthreads();
     // two centroids per step, each with even/odd partial max/min: eight
     // independent dependency chains per thread
 #pragma unroll 1
     for (int j = 0; j < cn; j += 2) {
       const bool two = j + 1 < cn;
-      const float4* ca = reinterpret_cast<const float4*>(cs + j * D + gi * kGroup);
-      const float4* cb = reinterpret_cast<const float4*>(cs + (two ? j + 1 : j) * D + gi * kGroup);
+      const float4* ca = reinterpret_cast<const float4*>(cs + j * RS + gi * GS);
+      const float4* cb = reinterpret_cast<const float4*>(cs + (two ? j + 1 : j) * RS + gi * GS);
       float ax0 = -INFINITY, ax1 = -INFINITY, an0 = INFINITY, an1 = INFINITY;
       float bx0 = -INFINITY, bx1 = -INFINITY, bn0 = INFINITY, bn1 = INFINITY;
 #pragma unroll
@@ -259,7 +263,7 @@ cudaError_t launch_t(const qwm_ctx* c, const void* k, const void* v, int64_t n, 
                      int32_t version, cudaStream_t st) {
   const int r = c->cfg.rank, H = c->cfg.heads, nC = c->cfg.n_centroids;
   constexpr int CH = 16384 / D;
-  const size_t smem = (size_t)CH * D * 4 + (size_t)r * D * 4;
+  const size_t smem = (size_t)CH * (D / kGroup) * (kGroup + 4) * 4 + (size_t)r * D * 4;
   auto kern = append_kernel<D, T>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

@@ -6,13 +6,16 @@
 //
 // One CTA owns 128 query rows of one head and streams every 128-slot tile of
 // that head.  Warp roles:
-//   warps 0-3   softmax: thread i owns query row i (TMEM lane i).  Reads S
+//   warps 0-3   softmax: thread i owns query row i (TMEM lane i).  Writes its
+//               Q row into TMEM once (the A operand of QK^T).  Reads S
 //               from TMEM, online softmax in the exp2 domain with a lazy
 //               rescale (O is corrected only when the running maximum grows
 //               by more than 2^8), writes P (fp16) into TMEM, final 1/l and
 //               store of O.
-//   warps 4-11  producers: load Q once (SW128 K-major smem), and per tile
-//               dequantise k_hat into two bf16 terms (hi + lo, SW128 K-major,
+//   warps 4-11  producers: one thread bulk-copies every packed tile
+//               (cp.async.bulk, mbarrier complete_tx) into a 2-stage shared
+//               ring two tiles ahead; all of them dequantise from shared
+//               memory k_hat into two bf16 terms (hi + lo, SW128 K-major,
 //               rows = keys), v_hat^T into fp16 (SW128 K-major, rows = d), e
 //               into a no-swizzle K-major fp16 tile; recompute Z = q U_t^T as
 //               two fp16 terms when the tile's basis slot changes.
@@ -21,7 +24,8 @@
 //               O      += P V_hat                                 (A = P in TMEM)
 //               S(t+1) is issued before PV(t) so the tensor core works while
 //               the softmax warps handle tile t.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P [384,448).
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P [384,448),
+// Q [448,512) (bf16 pairs).
 // Synchronisation: mbarriers (k_ready, v_ready, p_ready, s_free[2] arrived by
 // threads; s_done[2], pv_done by tcgen05.commit).  Every wait is bounded by
 // the SM clock; a timeout sets a device status bit and every role leaves its
@@ -37,7 +41,7 @@ constexpr int kD = 128;
 constexpr int kSoftWarps = 4, kProdWarps = 8;
 constexpr int kThreads = (kSoftWarps + kProdWarps + 1) * 32;   // 416
 constexpr int kProdThreads = kProdWarps * 32;
-constexpr uint32_t kColS0 = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kColS0 = 0, kColO = 256, kColP = 384, kColQ = 448;
 constexpr long long kWaitCycles = 1ll << 31;                    // ~1 s at 2 GHz
 constexpr uint32_t kDevTimeout = 0x4u;
 
@@ -76,6 +80,15 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 __device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count));
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}"
+               ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+// one-dimensional bulk copy global -> shared, completion counted on `bar`
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(su32(dst)), "l"(src), "r"(bytes), "r"(su32(bar)) : "memory");
 }
 __device__ __forceinline__ void bar_arrive(uint64_t* b) {
   asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}" ::"r"(su32(b)) : "memory");
@@ -182,15 +195,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   constexpr int G = kD / kGroup;
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024 - (su32(sm_raw) & 1023)) & 1023);
-  uint8_t* Qs = sm;                      // 32 KB
-  uint8_t* Khi = sm + 32768;             // 32 KB
-  uint8_t* Klo = sm + 65536;             // 32 KB
-  uint8_t* Vt = sm + 98304;              // 32 KB
-  uint8_t* Es = sm + 131072;             // 128 x RP fp16, core matrices
+  uint8_t* Khi = sm;                     // 32 KB
+  uint8_t* Klo = sm + 32768;             // 32 KB
+  uint8_t* Vt = sm + 65536;              // 32 KB
+  uint8_t* Es = sm + 98304;              // 128 x RP fp16, core matrices
   uint8_t* Zh = Es + 128 * RP * 2;       // 128 x RP fp16
   uint8_t* Zl = Zh + 128 * RP * 2;
-  uint8_t* Cs = Zl + 128 * RP * 2;       // C x 256 B (CS only)
-  __shared__ __align__(8) uint64_t bars[8];
+  uint8_t* Ring = Zl + 128 * RP * 2;     // 2 x tile bytes (packed tiles)
+  uint8_t* Cs = Ring + 2 * a.off.bytes;  // C x 256 B (CS only)
+  __shared__ __align__(8) uint64_t bars[11];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
   uint64_t* k_ready = &bars[0];
@@ -199,6 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   uint64_t* pv_done = &bars[3];
   uint64_t* s_done = &bars[4];   // [2]
   uint64_t* s_free = &bars[6];   // [2]
+  uint64_t* full = &bars[8];     // [2] packed tile landed in ring stage
+  uint64_t* q_ready = &bars[10];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
@@ -215,6 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     bar_init(&s_done[1], 1);
     bar_init(&s_free[0], 128);
     bar_init(&s_free[1], 128);
+    bar_init(&full[0], 1);
+    bar_init(&full[1], 1);
+    bar_init(q_ready, 128);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 12) {
@@ -232,6 +250,24 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     const float c2 = a.scale_log2;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
+    {
+      // this thread's Q row into TMEM columns [448, 512) as bf16 pairs
+      const int64_t grow = row0 + tid;
+      const uint4* src = reinterpret_cast<const uint4*>(a.Q + ((int64_t)h * a.M + grow) * kD);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint4 x = make_uint4(0, 0, 0, 0);
+          if (grow < a.M) x = src[8 * hf + i];
+          v[4 * i] = x.x; v[4 * i + 1] = x.y; v[4 * i + 2] = x.z; v[4 * i + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_base + kColQ + 32 * hf, v);
+      }
+      tmem_wait_st();
+      fence_before();
+      bar_arrive(q_ready);
+    }
     for (int64_t t = 0; t < nt && ok; ++t) {
       const int b = (int)(t & 1);
       const int nv = a.tiles[t].y;
@@ -321,31 +357,27 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     // ------------------------------------------------------------ producers
     const int p = tid - kSoftWarps * 32;      // 0..255
     const __nv_bfloat16* ch = a.cent + (int64_t)h * a.nC * kD;
-    // Q rows into SW128 K-major smem: thread (row, half) copies 64 channels
-    {
-      const int row = p & 127, half = p >> 7;
-      const int64_t grow = row0 + row;
-      const __nv_bfloat16* src = a.Q + ((int64_t)h * a.M + grow) * kD + half * 64;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (grow < a.M) val = *reinterpret_cast<const uint4*>(src + 8 * c);
-        *reinterpret_cast<uint4*>(Qs + sw128_off(row, half * 8 + c)) = val;
-      }
-    }
     if (CS) {
       for (int i = p; i < a.nC * 16; i += kProdThreads) {
         const int j = i >> 4, c = i & 15;
         *reinterpret_cast<uint4*>(Cs + cswz(j, c)) = *reinterpret_cast<const uint4*>(ch + (int64_t)j * kD + 8 * c);
       }
     }
-    prod_sync();
     int cur_slot = -1;
     bool ok = true;
+    const uint32_t TB = (uint32_t)a.off.bytes;
     const uint8_t* tiles_h = a.cache + (int64_t)h * a.max_tiles * a.off.bytes;
+    if (p == 0) {
+      for (int64_t u = 0; u < 2 && u < nt; ++u) {
+        bar_expect_tx(&full[u], TB);
+        bulk_g2s(Ring + u * TB, tiles_h + u * TB, TB, &full[u]);
+      }
+    }
+    prod_sync();
     for (int64_t t = 0; t < nt && ok; ++t) {
-      const uint8_t* tb = tiles_h + t * a.off.bytes;
+      const uint8_t* tb = Ring + (t & 1) * TB;
       const int slot = a.tiles[t].x;
+      if (!prod_all(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       if (t > 0) {
         if (!prod_all(bar_wait(&s_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       }
@@ -361,8 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
             float z[RP];
 #pragma unroll
             for (int i = 0; i < RP; ++i) z[i] = 0.f;
+            const int64_t grow = row0 + p;
+            const uint4* qrow = reinterpret_cast<const uint4*>(a.Q + ((int64_t)h * a.M + grow) * kD);
             for (int c8 = 0; c8 < 16; ++c8) {
-              const uint4 qv = *reinterpret_cast<const uint4*>(Qs + sw128_off(p, c8));
+              const uint4 qv = grow < a.M ? qrow[c8] : make_uint4(0, 0, 0, 0);
               const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
@@ -488,12 +522,20 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       }
       fence_async_smem();
       bar_arrive(v_ready);
+      // every producer is done with ring stage t & 1: refill it with tile t + 2
+      prod_sync();
+      if (p == 0 && t + 2 < nt) {
+        bar_expect_tx(&full[t & 1], TB);
+        bulk_g2s(Ring + (t & 1) * TB, tiles_h + (t + 2) * TB, TB, &full[t & 1]);
+      }
     }
   } else {
     // ------------------------------------------------------------ MMA issuer
     const bool leader = lane == 0;
     bool ok = true;
-    const uint32_t qa = su32(Qs), kh = su32(Khi), kl = su32(Klo), vt = su32(Vt);
+    const uint32_t kh = su32(Khi), kl = su32(Klo), vt = su32(Vt);
+    ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
+    fence_after();
     const uint32_t ea = su32(Es), za = su32(Zh), zl = su32(Zl);
     constexpr uint32_t kSbo = (RP / 8) * 128;
     for (int64_t t = 0; t <= nt && ok; ++t) {
@@ -507,12 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-            mma_ss(d, desc_sw128(qa + ko), desc_sw128(kh + ko), kIdescQK, j > 0);
+            mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kh + ko), kIdescQK, j > 0);
           }
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-            mma_ss(d, desc_sw128(qa + ko), desc_sw128(kl + ko), kIdescQK, 1);
+            mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kl + ko), kIdescQK, 1);
           }
           if constexpr (RP > 0) {
 #pragma unroll
@@ -552,7 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
 }
 
 size_t tc_smem(const qwm_ctx* c, int RP, bool cs) {
-  return 1024 + 4 * 32768 + 3 * (size_t)128 * RP * 2 + (cs ? (size_t)c->cfg.n_centroids * 256 : 0);
+  return 1024 + 3 * 32768 + 3 * (size_t)128 * RP * 2 + 2 * c->lay.tile_bytes +
+         (cs ? (size_t)c->cfg.n_centroids * 256 : 0);
 }
 
 template <int RP, bool CS>

@@ -299,6 +299,7 @@ extern "C" qwm_status qwm_set_attend_kernel(qwm_ctx* x, int32_t k) {
 extern "C" int32_t qwm_resolved_attend_kernel(const qwm_ctx* x) {
   if (!x) return -1;
   if (x->attend_kernel != 0) return x->attend_kernel;
+  if (attend_tc_supported(x)) return 3;
   return attend_mma_supported(x) ? 2 : 1;
 }
 

@@ -220,9 +220,9 @@ qwm_status qwm_kmeans(int32_t heads, int32_t head_dim, int32_t dtype, int32_t n_
                       const void* d_keys, int64_t n, const int32_t* d_init_rows, int32_t iters,
                       void* d_centroids, void* d_workspace, void* stream);
 
-/* Attention kernel choice: 0 = automatic (tensor-core kernel where it
- * applies), 1 = float32 CUDA-core kernel, 2 = bf16 mma.sync kernel,
- * 3 = bf16 tcgen05 kernel. */
+/* Attention kernel choice: 0 = automatic (the tcgen05 kernel for bf16,
+ * d = 128, r <= 32; else the CUDA-core kernel), 1 = float32 CUDA-core kernel,
+ * 2 = bf16 mma.sync kernel, 3 = bf16 tcgen05 kernel. */
 qwm_status qwm_set_attend_kernel(qwm_ctx* ctx, int32_t kernel);
 
 /* The attention kernel qwm_attend will run (1, 2 or 3; automatic resolved). */

@@ -169,7 +169,7 @@ def test_attend_full_size_bench_configuration(qwm):
     wl, ctx, cent, bases = _build(qwm, name, list(range(12)), [wl_chunk for wl_chunk in [4680] * 7])
     q = synth.queries(wl, 0)
     got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
-    assert ctx.resolved_attend_kernel == 2
+    assert ctx.resolved_attend_kernel == 3
     rows = np.sort(np.random.default_rng(5).choice(wl.n_query, 48, replace=False))
     qs = q[:, rows]
     want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, qs, [0, 11], 1 / np.sqrt(128))
