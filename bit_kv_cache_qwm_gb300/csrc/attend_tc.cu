@@ -16,7 +16,8 @@
 //               (cp.async.bulk, mbarrier complete_tx) into a 2-stage shared
 //               ring two tiles ahead; all of them dequantise from shared
 //               memory k_hat into two bf16 terms (hi + lo, SW128 K-major,
-//               rows = keys), v_hat^T into fp16 (SW128 K-major, rows = d), e
+//               rows = keys), v_hat into fp16 (the same layout, read by the PV
+//               MMA as an MN-major operand), e
 //               into a no-swizzle K-major fp16 tile; recompute Z = q U_t^T as
 //               two fp16 terms when the tile's basis slot changes.
 //   warp 12     MMA issuer (one lane) and TMEM owner:
@@ -47,11 +48,17 @@ constexpr uint32_t kDevTimeout = 0x4u;
 
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | (16u << 17) | (8u << 24);  // bf16 x bf16 -> f32
 constexpr uint32_t kIdescF16 = (1u << 4) | (16u << 17) | (8u << 24);                           // f16 x f16 -> f32
+constexpr uint32_t kIdescPV = kIdescF16 | (1u << 16);                                          // B MN-major
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | (1ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
+}
+// SW128 MN-major: 64 MN-elements x 8 K-rows per 1 KiB atom; lbo = next 64 MN
+// (16 KiB here), sbo = next 8 K-rows (1 KiB)
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | (1024ull << 16) | (64ull << 32) | (1ull << 46) | (2ull << 61);
 }
 // no-swizzle K-major: core matrices of 8 rows x 16 B; lbo = next core along K,
 // sbo = next core along M/N
@@ -495,29 +502,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
         if (!prod_all(bar_wait(pv_done, (uint32_t)((t - 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       }
       {
-        const int kb = p & 15, cb = p >> 4;          // keys 8kb.., channels 8cb..
-        const int g = cb >> 2;
-        float vv[8][8];                              // [key][channel]
+        // v_hat rows (thread = key, 64 channels), stored like k_hat; the PV
+        // MMA reads this tile as an MN-major B operand
+        const int key = p & 127, half = p >> 7;
+        const uint4 vc = *reinterpret_cast<const uint4*>(tb + a.off.vcode + key * 32 + half * 16);
+        const uint2 vq = *reinterpret_cast<const uint2*>(tb + a.off.vqp + (key * G + 2 * half) * 4);
+        const uint32_t vw[4] = {vc.x, vc.y, vc.z, vc.w};
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int key = 8 * kb + kk;
-          const uint32_t bits = *reinterpret_cast<const uint16_t*>(tb + a.off.vcode + key * 32 + 2 * cb);
-          const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.vqp + (key * G + g) * 4);
+        for (int gg = 0; gg < 2; ++gg) {
+          const uint32_t qp = gg ? vq.y : vq.x;
           const float vz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
           const float vs = __half2float(__ushort_as_half((unsigned short)(qp >> 16)));
 #pragma unroll
-          for (int e = 0; e < 8; ++e) vv[kk][e] = fmaf((float)((bits >> (2 * e)) & 3u), vs, vz);
-        }
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const int chunk = half * 8 + gg * 4 + c8;
+            const uint32_t bits = (vw[gg * 2 + (c8 >> 1)] >> (16 * (c8 & 1))) & 0xffffu;
+            uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int dch = 8 * cb + e;
-          uint32_t w[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const __half2 hh = __floats2half2_rn(vv[2 * q][e], vv[2 * q + 1][e]);
-            w[q] = *reinterpret_cast<const uint32_t*>(&hh);
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const __half2 hh = __floats2half2_rn(fmaf((float)((bits >> (4 * e2)) & 3u), vs, vz),
+                                                   fmaf((float)((bits >> (4 * e2 + 2)) & 3u), vs, vz));
+              w[e2] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+            *reinterpret_cast<uint4*>(Vt + sw128_off(key, chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
-          *reinterpret_cast<uint4*>(Vt + sw128_off(dch, kb)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       fence_async_smem();
@@ -575,8 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
         if (leader) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-            mma_ts(tmem + kColO, tmem + kColP + 8 * j, desc_sw128(vt + ko), kIdescF16, (u > 0 || j > 0) ? 1u : 0u);
+            mma_ts(tmem + kColO, tmem + kColP + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV, (u > 0 || j > 0) ? 1u : 0u);
           }
           commit(pv_done);
         }
