@@ -151,6 +151,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -212,6 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   uint8_t* Cs = Ring + 2 * a.off.bytes;  // C x 256 B (CS only)
   __shared__ __align__(8) uint64_t bars[11];
   __shared__ uint32_t tmem_base_sh;
+  __shared__ float2 code_f2[16];      // (c0, c1) of a 4-bit pair of 2-bit codes
+  __shared__ __half2 code_h2[16];
   __shared__ volatile int abort_sh;
   uint64_t* k_ready = &bars[0];
   uint64_t* v_ready = &bars[1];
@@ -227,6 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   const int64_t row0 = (int64_t)blockIdx.x * 128;
   const int64_t nt = a.n_tiles;
 
+  if (tid < 16) {
+    code_f2[tid] = make_float2((float)(tid & 3), (float)(tid >> 2));
+    code_h2[tid] = __floats2half2_rn((float)(tid & 3), (float)(tid >> 2));
+  }
   if (tid == 0) {
     abort_sh = 0;
     bar_init(k_ready, kProdThreads);
@@ -282,13 +293,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       fence_after();
       const uint32_t sbase = tmem + lane_base + kColS0 + 128u * b;
       float mx = -INFINITY;
+      const bool ragged = nv < 128;
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t v[32];
         tmem_ld32(sbase + 32 * cb, v);
         tmem_wait_ld();
+        if (!ragged) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (32 * cb + i < nv) mx = fmaxf(mx, __uint_as_float(v[i]));
+          for (int i = 0; i < 32; i += 2) mx = max3f(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * cb + i < nv) mx = fmaxf(mx, __uint_as_float(v[i]));
+        }
       }
       const float mnew = fmaxf(m_run, mx * c2);
       if (t > 0) {
@@ -311,23 +328,28 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
         l_run *= corr;
       }
       if (need) m_run = mnew;
-      float psum = 0.f;
+      float2 psum2 = make_float2(0.f, 0.f);
+      const float2 c2v = make_float2(c2, c2), mv = make_float2(-m_run, -m_run);
       for (int cb = 0; cb < 4; ++cb) {
         uint32_t v[32], pk[16];
         tmem_ld32(sbase + 32 * cb, v);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int k0 = 32 * cb + 2 * i;
-          const float p0 = k0 < nv ? ex2(fmaf(__uint_as_float(v[2 * i]), c2, -m_run)) : 0.f;
-          const float p1 = k0 + 1 < nv ? ex2(fmaf(__uint_as_float(v[2 * i + 1]), c2, -m_run)) : 0.f;
-          const __half2 hp = __floats2half2_rn(p0, p1);
-          const float2 back = __half22float2(hp);
-          psum += back.x + back.y;
+          const float2 arg = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), c2v, mv);
+          float2 pp = make_float2(ex2(arg.x), ex2(arg.y));
+          if (ragged) {
+            const int k0 = 32 * cb + 2 * i;
+            pp.x = k0 < nv ? pp.x : 0.f;
+            pp.y = k0 + 1 < nv ? pp.y : 0.f;
+          }
+          psum2 = __fadd2_rn(psum2, pp);
+          const __half2 hp = __floats2half2_rn(pp.x, pp.y);
           pk[i] = *reinterpret_cast<const uint32_t*>(&hp);
         }
         tmem_st16(tmem + lane_base + kColP + 16 * cb, pk);
       }
+      const float psum = psum2.x + psum2.y;
       tmem_wait_st();
       l_run += psum;
       fence_before();
@@ -445,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
           const uint32_t qp = gg ? kq.y : kq.x;
           const float kz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
           const float ks = __half2float(__ushort_as_half((unsigned short)(qp >> 16)));
+          const float2 kz2 = make_float2(kz, kz), ks2 = make_float2(ks, ks);
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {
             const int chunk = half * 8 + gg * 4 + c8;          // 8-channel chunk 0..15
@@ -456,17 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
             uint32_t ph[4], pl[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
-              float kv[2];
-#pragma unroll
-              for (int u = 0; u < 2; ++u) {
-                const int e = 2 * e2 + u;
-                const float code = (float)((bits >> (2 * e)) & 3u);
-                const float cval = __uint_as_float(u ? (cw[e2] & 0xffff0000u) : (cw[e2] << 16));
-                kv[u] = cval + fmaf(code, ks, kz);
-              }
-              const __nv_bfloat162 hb = __floats2bfloat162_rn(kv[0], kv[1]);
+              const float2 cd = code_f2[(bits >> (4 * e2)) & 15u];
+              const float2 rq = __ffma2_rn(cd, ks2, kz2);                      // zero + code*scale
+              const float2 cc = make_float2(__uint_as_float(cw[e2] << 16), __uint_as_float(cw[e2] & 0xffff0000u));
+              const float2 kv = __fadd2_rn(cc, rq);                            // + centroid
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(kv.x, kv.y);
               const float2 hf = __bfloat1622float2(hb);
-              const __nv_bfloat162 lb = __floats2bfloat162_rn(kv[0] - hf.x, kv[1] - hf.y);
+              const float2 lo = __fadd2_rn(kv, make_float2(-hf.x, -hf.y));
+              const __nv_bfloat162 lb = __floats2bfloat162_rn(lo.x, lo.y);
               ph[e2] = *reinterpret_cast<const uint32_t*>(&hb);
               pl[e2] = *reinterpret_cast<const uint32_t*>(&lb);
             }
@@ -511,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
 #pragma unroll
         for (int gg = 0; gg < 2; ++gg) {
           const uint32_t qp = gg ? vq.y : vq.x;
-          const float vz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
-          const float vs = __half2float(__ushort_as_half((unsigned short)(qp >> 16)));
+          const __half2 vz2 = __half2half2(__ushort_as_half((unsigned short)(qp & 0xffffu)));
+          const __half2 vs2 = __half2half2(__ushort_as_half((unsigned short)(qp >> 16)));
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {
             const int chunk = half * 8 + gg * 4 + c8;
@@ -520,8 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
             uint32_t w[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
-              const __half2 hh = __floats2half2_rn(fmaf((float)((bits >> (4 * e2)) & 3u), vs, vz),
-                                                   fmaf((float)((bits >> (4 * e2 + 2)) & 3u), vs, vz));
+              const __half2 hh = __hfma2(code_h2[(bits >> (4 * e2)) & 15u], vs2, vz2);   // zero + code*scale
               w[e2] = *reinterpret_cast<const uint32_t*>(&hh);
             }
             *reinterpret_cast<uint4*>(Vt + sw128_off(key, chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
