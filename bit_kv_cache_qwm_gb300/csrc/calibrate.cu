@@ -183,83 +183,6 @@ __device__ int jacobi(float* A, int lda, float* V, int ldv, int n, int max_sweep
   return sweep + 1;
 }
 
-// The same Jacobi iteration run by one warp (n <= 32): __syncwarp instead of
-// block barriers, so a step costs a few dozen cycles.  Lanes 0..31 only.
-__device__ int jacobi_warp(float* A, int lda, float* V, int ldv, int n, int max_sweeps, float* rot,
-                           int* prs) {
-  const int lane = threadIdx.x & 31;
-  const int ne = n + (n & 1), half = ne / 2;
-  int sweep = 0;
-  for (; sweep < max_sweeps; ++sweep) {
-    int rotated = 0;
-    for (int k = 0; k < ne - 1; ++k) {
-      if (lane < half) {
-        int p, q;
-        rr_pair(ne, k, lane, &p, &q);
-        float c = 1.f, s = 0.f;
-        if (p < n && q < n) {
-          const float app = A[p * lda + p], aqq = A[q * lda + q], apq = A[p * lda + q];
-          if (apq != 0.f && fabsf(apq) > 9.5367431640625e-07f * sqrtf(fabsf(app * aqq))) {
-            const float th = (app - aqq) / (2.f * apq);
-            const float t = (th >= 0.f ? -1.f : 1.f) / (fabsf(th) + sqrtf(th * th + 1.f));
-            c = 1.f / sqrtf(t * t + 1.f);
-            s = t * c;
-            rotated = 1;
-          }
-        }
-        rot[2 * lane] = c;
-        rot[2 * lane + 1] = s;
-        prs[2 * lane] = p;
-        prs[2 * lane + 1] = q;
-      }
-      __syncwarp();
-      for (int idx = lane; idx < half * half; idx += 32) {
-        const int a = idx / half, b = idx % half;
-        const int p1 = prs[2 * a], q1 = prs[2 * a + 1], p2 = prs[2 * b], q2 = prs[2 * b + 1];
-        const float c1 = rot[2 * a], s1 = rot[2 * a + 1], c2 = rot[2 * b], s2 = rot[2 * b + 1];
-        const bool vp1 = p1 < n, vq1 = q1 < n, vp2 = p2 < n, vq2 = q2 < n;
-        const float m00 = (vp1 && vp2) ? A[p1 * lda + p2] : 0.f;
-        const float m01 = (vp1 && vq2) ? A[p1 * lda + q2] : 0.f;
-        const float m10 = (vq1 && vp2) ? A[q1 * lda + p2] : 0.f;
-        const float m11 = (vq1 && vq2) ? A[q1 * lda + q2] : 0.f;
-        const float t00 = c1 * m00 - s1 * m10, t01 = c1 * m01 - s1 * m11;
-        const float t10 = s1 * m00 + c1 * m10, t11 = s1 * m01 + c1 * m11;
-        if (vp1 && vp2) A[p1 * lda + p2] = t00 * c2 - t01 * s2;
-        if (vp1 && vq2) A[p1 * lda + q2] = t00 * s2 + t01 * c2;
-        if (vq1 && vp2) A[q1 * lda + p2] = t10 * c2 - t11 * s2;
-        if (vq1 && vq2) A[q1 * lda + q2] = t10 * s2 + t11 * c2;
-      }
-      for (int idx = lane; idx < n * half; idx += 32) {
-        const int i = idx / half, a = idx % half;
-        const int p = prs[2 * a], q = prs[2 * a + 1];
-        if (p < n && q < n) {
-          const float c = rot[2 * a], s = rot[2 * a + 1];
-          const float vp = V[i * ldv + p], vq = V[i * ldv + q];
-          V[i * ldv + p] = c * vp - s * vq;
-          V[i * ldv + q] = s * vp + c * vq;
-        }
-      }
-      __syncwarp();
-    }
-    if (!__any_sync(0xffffffffu, rotated)) break;
-  }
-  return sweep + 1;
-}
-
-// Jacobi on an m x m projected matrix: one warp when m <= 32, else the block.
-__device__ int jacobi_small(float* A, int lda, float* V, int ldv, int n, int max_sweeps, float* rot,
-                            int* prs) {
-  int sweeps = 0;
-  if (n <= 32) {
-    __syncthreads();
-    if (threadIdx.x < 32) sweeps = jacobi_warp(A, lda, V, ldv, n, max_sweeps, rot, prs);
-    __syncthreads();
-  } else {
-    sweeps = jacobi(A, lda, V, ldv, n, max_sweeps, rot, prs);
-  }
-  return sweeps;
-}
-
 // Modified Gram-Schmidt, twice, on the m <= 64 columns of X (d rows, leading
 // dim ldx).  Column k lives in the registers of warp k % 8 (d/32 values per
 // lane); the owner of column j normalises it and publishes it through a
@@ -558,8 +481,7 @@ eig_kernel(const float* __restrict__ part, int splits, int64_t n_h, int r, int m
   if (!full) matmul_ax(A, L.ldg, A, L.ldg, A2, L.ldg, D, D);   // iterate on A^2
   while (true) {
     if (!full) {
-      const int block_iters = iters == 0 ? 2 * kCheckEvery : kCheckEvery;
-      for (int t = 0; t < block_iters && iters < max_iter; ++t, ++iters) {
+      for (int t = 0; t < kCheckEvery && iters < max_iter; ++t, ++iters) {
         matmul_ax(A2, L.ldg, X, L.ldm, W, L.ldm, D, m);
         for (int idx = tid; idx < D * m; idx += blockDim.x)
           X[(idx / m) * L.ldm + idx % m] = W[(idx / m) * L.ldm + idx % m];
@@ -570,7 +492,7 @@ eig_kernel(const float* __restrict__ part, int splits, int64_t n_h, int r, int m
       matmul_ax(A, L.ldg, X, L.ldm, W, L.ldm, D, m);
       project(X, L.ldm, W, L.ldm, Hm, L.ldm, D, m);
       set_identity(V, L.ldm, m);
-      jacobi_small(Hm, L.ldm, V, L.ldm, m, 12, rot, prs);
+      jacobi(Hm, L.ldm, V, L.ldm, m, 12, rot, prs);
       rotate_sorted(X, L.ldm, D, m, V, L.ldm, Hm, L.ldm, theta, order, wbuf);
     }
     // second pass on the re-orthonormalised Ritz vectors
@@ -579,7 +501,7 @@ eig_kernel(const float* __restrict__ part, int splits, int64_t n_h, int r, int m
     matmul_ax(A, L.ldg, X, L.ldm, W, L.ldm, D, m);
     project(X, L.ldm, W, L.ldm, Hm, L.ldm, D, m);
     set_identity(V, L.ldm, m);
-    jacobi_small(Hm, L.ldm, V, L.ldm, m, 4, rot, prs);
+    jacobi(Hm, L.ldm, V, L.ldm, m, 4, rot, prs);
     rotate_sorted(X, L.ldm, D, m, V, L.ldm, Hm, L.ldm, theta, order, wbuf);
     rotate_sorted(W, L.ldm, D, m, V, L.ldm, Hm, L.ldm, theta, order, wbuf);
     // residuals of the leading r Ritz pairs
