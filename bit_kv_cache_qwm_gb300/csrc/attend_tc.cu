@@ -21,14 +21,17 @@
 //               into a no-swizzle K-major fp16 tile; recompute Z = q U_t^T as
 //               two fp16 terms when the tile's basis slot changes.
 //   warp 12     MMA issuer (one lane) and TMEM owner:
-//               S[t&1]  = Q khi^T + Q klo^T + Zhi E^T + Zlo E^T   (M=128, N=128)
-//               O      += P V_hat                                 (A = P in TMEM)
-//               S(t+1) is issued before PV(t) so the tensor core works while
-//               the softmax warps handle tile t.
+//               S[t&1]  = Q khi^T + Q klo^T + Zhi E^T + Zlo E^T   (M=128)
+//               in two halves of 64 keys (N=64 each), so the producers
+//               dequantise one half while the tensor core multiplies the
+//               other, and O += P V_hat (A = P in TMEM).  The issuer probes
+//               the ready barriers without blocking and issues whatever is
+//               ready, in order within each stream.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P [384,448),
 // Q [448,512) (bf16 pairs).
-// Synchronisation: mbarriers (k_ready, v_ready, p_ready, s_free[2] arrived by
-// threads; s_done[2], pv_done by tcgen05.commit).  Every wait is bounded by
+// Synchronisation: mbarriers (kA_ready, kB_ready, v_ready, p_ready, s_free[2],
+// q_ready arrived by threads; sA_done[2], sB_done[2], pv_done by
+// tcgen05.commit; full[2] by the bulk copies).  Every wait is bounded by
 // the SM clock; a timeout sets a device status bit and every role leaves its
 // loop, the TMEM is freed and the kernel returns.
 #include <math.h>
@@ -49,6 +52,9 @@ constexpr uint32_t kDevTimeout = 0x4u;
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | (16u << 17) | (8u << 24);  // bf16 x bf16 -> f32
 constexpr uint32_t kIdescF16 = (1u << 4) | (16u << 17) | (8u << 24);                           // f16 x f16 -> f32
 constexpr uint32_t kIdescPV = kIdescF16 | (1u << 16);                                          // B MN-major
+// N = 64 halves of the S tile
+constexpr uint32_t kIdescQK64 = (1u << 4) | (1u << 7) | (1u << 10) | (8u << 17) | (8u << 24);
+constexpr uint32_t kIdescF16_64 = (1u << 4) | (8u << 17) | (8u << 24);
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -128,6 +134,31 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* v) {
                  "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
                  "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
                  "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+               : "r"(taddr));
+}
+// non-blocking probe of a phase (no suspend)
+__device__ __forceinline__ bool bar_test(uint64_t* b, uint32_t par) {
+  uint32_t done;
+  asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+               "selp.u32 %0, 1, 0, p;\n}"
+               : "=r"(done) : "r"(su32(b)), "r"(par) : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t* v) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+               "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,"
+               "%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,"
+               "%60,%61,%62,%63}, [%64];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+                 "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+                 "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+                 "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+                 "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31]), "=r"(v[32]), "=r"(v[33]), "=r"(v[34]),
+                 "=r"(v[35]), "=r"(v[36]), "=r"(v[37]), "=r"(v[38]), "=r"(v[39]), "=r"(v[40]), "=r"(v[41]),
+                 "=r"(v[42]), "=r"(v[43]), "=r"(v[44]), "=r"(v[45]), "=r"(v[46]), "=r"(v[47]), "=r"(v[48]),
+                 "=r"(v[49]), "=r"(v[50]), "=r"(v[51]), "=r"(v[52]), "=r"(v[53]), "=r"(v[54]), "=r"(v[55]),
+                 "=r"(v[56]), "=r"(v[57]), "=r"(v[58]), "=r"(v[59]), "=r"(v[60]), "=r"(v[61]), "=r"(v[62]),
+                 "=r"(v[63])
                : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
@@ -215,19 +246,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   uint8_t* Zl = Zh + 128 * RP * 2;
   uint8_t* Ring = Zl + 128 * RP * 2;     // 2 x tile bytes (packed tiles)
   uint8_t* Cs = Ring + 2 * a.off.bytes;  // C x 256 B (CS only)
-  __shared__ __align__(8) uint64_t bars[11];
+  __shared__ __align__(8) uint64_t bars[14];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float2 code_f2[16];      // (c0, c1) of a 4-bit pair of 2-bit codes
   __shared__ __half2 code_h2[16];
   __shared__ volatile int abort_sh;
-  uint64_t* k_ready = &bars[0];
-  uint64_t* v_ready = &bars[1];
-  uint64_t* p_ready = &bars[2];
-  uint64_t* pv_done = &bars[3];
-  uint64_t* s_done = &bars[4];   // [2]
-  uint64_t* s_free = &bars[6];   // [2]
-  uint64_t* full = &bars[8];     // [2] packed tile landed in ring stage
-  uint64_t* q_ready = &bars[10];
+  uint64_t* kA_ready = &bars[0];  // keys 0-63 of k_hat (and their e) written
+  uint64_t* kB_ready = &bars[1];  // keys 64-127
+  uint64_t* v_ready = &bars[2];
+  uint64_t* p_ready = &bars[3];
+  uint64_t* pv_done = &bars[4];
+  uint64_t* sA_done = &bars[5];   // [2] per S buffer: first half of S(t) computed
+  uint64_t* sB_done = &bars[7];   // [2] whole S(t) computed
+  uint64_t* s_free = &bars[9];    // [2]
+  uint64_t* full = &bars[11];     // [2] packed tile landed in ring stage
+  uint64_t* q_ready = &bars[13];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
@@ -240,16 +273,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   }
   if (tid == 0) {
     abort_sh = 0;
-    bar_init(k_ready, kProdThreads);
+    bar_init(kA_ready, kProdThreads);
+    bar_init(kB_ready, kProdThreads);
     bar_init(v_ready, kProdThreads);
     bar_init(p_ready, 128);
     bar_init(pv_done, 1);
-    bar_init(&s_done[0], 1);
-    bar_init(&s_done[1], 1);
-    bar_init(&s_free[0], 128);
-    bar_init(&s_free[1], 128);
-    bar_init(&full[0], 1);
-    bar_init(&full[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      bar_init(&sA_done[i], 1);
+      bar_init(&sB_done[i], 1);
+      bar_init(&s_free[i], 128);
+      bar_init(&full[i], 1);
+    }
     bar_init(q_ready, 128);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -289,22 +323,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     for (int64_t t = 0; t < nt && ok; ++t) {
       const int b = (int)(t & 1);
       const int nv = a.tiles[t].y;
-      if (!warp_all(bar_wait(&s_done[b], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
+      if (!warp_all(bar_wait(&sB_done[b], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       fence_after();
       const uint32_t sbase = tmem + lane_base + kColS0 + 128u * b;
       float mx = -INFINITY;
       const bool ragged = nv < 128;
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t v[32];
-        tmem_ld32(sbase + 32 * cb, v);
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t v[64];
+        tmem_ld64(sbase + 64 * cb, v);
         tmem_wait_ld();
         if (!ragged) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) mx = max3f(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+          for (int i = 0; i < 64; i += 2) mx = max3f(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (32 * cb + i < nv) mx = fmaxf(mx, __uint_as_float(v[i]));
+          for (int i = 0; i < 64; ++i)
+            if (64 * cb + i < nv) mx = fmaxf(mx, __uint_as_float(v[i]));
         }
       }
       const float mnew = fmaxf(m_run, mx * c2);
@@ -330,16 +364,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       if (need) m_run = mnew;
       float2 psum2 = make_float2(0.f, 0.f);
       const float2 c2v = make_float2(c2, c2), mv = make_float2(-m_run, -m_run);
-      for (int cb = 0; cb < 4; ++cb) {
-        uint32_t v[32], pk[16];
-        tmem_ld32(sbase + 32 * cb, v);
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t v[64], pk[32];
+        tmem_ld64(sbase + 64 * cb, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 32; ++i) {
           const float2 arg = __ffma2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), c2v, mv);
           float2 pp = make_float2(ex2(arg.x), ex2(arg.y));
           if (ragged) {
-            const int k0 = 32 * cb + 2 * i;
+            const int k0 = 64 * cb + 2 * i;
             pp.x = k0 < nv ? pp.x : 0.f;
             pp.y = k0 + 1 < nv ? pp.y : 0.f;
           }
@@ -347,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
           const __half2 hp = __floats2half2_rn(pp.x, pp.y);
           pk[i] = *reinterpret_cast<const uint32_t*>(&hp);
         }
-        tmem_st16(tmem + lane_base + kColP + 16 * cb, pk);
+        tmem_st32(tmem + lane_base + kColP + 32 * cb, pk);
       }
       const float psum = psum2.x + psum2.y;
       tmem_wait_st();
@@ -407,75 +441,77 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
       const uint8_t* tb = Ring + (t & 1) * TB;
       const int slot = a.tiles[t].x;
       if (!prod_all(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
-      if (t > 0) {
-        if (!prod_all(bar_wait(&s_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
-      }
-      if constexpr (RP > 0) {
-        if (slot != cur_slot) {
-          cur_slot = slot;
-          // stage U (fp32 [r][128]) in the free khi buffer, then Z = q U^T
-          float* Us = reinterpret_cast<float*>(Khi);
-          const float* U = a.basis + ((int64_t)slot * a.H + h) * a.r * kD;
-          for (int i = p; i < RP * kD; i += kProdThreads) Us[i] = (i / kD) < a.r ? U[i] : 0.f;
-          prod_sync();
-          if (p < 128) {
-            float z[RP];
-#pragma unroll
-            for (int i = 0; i < RP; ++i) z[i] = 0.f;
-            const int64_t grow = row0 + p;
-            const uint4* qrow = reinterpret_cast<const uint4*>(a.Q + ((int64_t)h * a.M + grow) * kD);
-            for (int c8 = 0; c8 < 16; ++c8) {
-              const uint4 qv = grow < a.M ? qrow[c8] : make_uint4(0, 0, 0, 0);
-              const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const float qf = __uint_as_float(e & 1 ? (qw[e >> 1] & 0xffff0000u) : (qw[e >> 1] << 16));
-                const int c = 8 * c8 + e;
-#pragma unroll
-                for (int i = 0; i < RP; ++i) z[i] = fmaf(qf, Us[i * kD + c], z[i]);
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < RP / 8; ++j) {
-              uint32_t hw[4], lw[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __half h0 = __float2half_rn(z[8 * j + 2 * e]), h1 = __float2half_rn(z[8 * j + 2 * e + 1]);
-                const __half2 hh = __halves2half2(h0, h1);
-                const __half2 ll = __floats2half2_rn(z[8 * j + 2 * e] - __half2float(h0),
-                                                     z[8 * j + 2 * e + 1] - __half2float(h1));
-                hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
-                lw[e] = *reinterpret_cast<const uint32_t*>(&ll);
-              }
-              const int off = ((p >> 3) * (RP / 8) + j) * 128 + (p & 7) * 16;
-              *reinterpret_cast<uint4*>(Zh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-              *reinterpret_cast<uint4*>(Zl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-          }
-          prod_sync();
+      for (int hk = 0; hk < 2; ++hk) {
+        // half hk (keys 64hk .. 64hk+63) of S(t-1) must be computed before
+        // its k_hat rows are overwritten
+        if (t > 0) {
+          uint64_t* prev = hk == 0 ? &sA_done[(t - 1) & 1] : &sB_done[(t - 1) & 1];
+          if (!prod_all(bar_wait(prev, (uint32_t)(((t - 1) >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
         }
-      }
-      // ---- k_hat (hi, lo) and e ----
-      {
-        const int key = p & 127, half = p >> 7;
-        const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
-        const uint4 kc = *reinterpret_cast<const uint4*>(tb + a.off.kcode + key * 32 + half * 16);
-        const uint2 kq = *reinterpret_cast<const uint2*>(tb + a.off.kqp + (key * G + 2 * half) * 4);
-        const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
+        if constexpr (RP > 0) {
+          if (hk == 0 && slot != cur_slot) {
+            cur_slot = slot;
+            // Z and all of khi are read by both halves of S(t-1)
+            if (t > 0 && !prod_all(bar_wait(&sB_done[(t - 1) & 1], (uint32_t)(((t - 1) >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
+            // stage U (fp32 [r][128]) in the free khi buffer, then Z = q U^T
+            float* Us = reinterpret_cast<float*>(Khi);
+            const float* U = a.basis + ((int64_t)slot * a.H + h) * a.r * kD;
+            for (int i = p; i < RP * kD; i += kProdThreads) Us[i] = (i / kD) < a.r ? U[i] : 0.f;
+            prod_sync();
+            if (p < 128) {
+              float z[RP];
 #pragma unroll
-        for (int gg = 0; gg < 2; ++gg) {
-          const uint32_t qp = gg ? kq.y : kq.x;
+              for (int i = 0; i < RP; ++i) z[i] = 0.f;
+              const int64_t grow = row0 + p;
+              const uint4* qrow = reinterpret_cast<const uint4*>(a.Q + ((int64_t)h * a.M + grow) * kD);
+              for (int c8 = 0; c8 < 16; ++c8) {
+                const uint4 qv = grow < a.M ? qrow[c8] : make_uint4(0, 0, 0, 0);
+                const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const float qf = __uint_as_float(e & 1 ? (qw[e >> 1] & 0xffff0000u) : (qw[e >> 1] << 16));
+                  const int c = 8 * c8 + e;
+#pragma unroll
+                  for (int i = 0; i < RP; ++i) z[i] = fmaf(qf, Us[i * kD + c], z[i]);
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < RP / 8; ++j) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const __half h0 = __float2half_rn(z[8 * j + 2 * e]), h1 = __float2half_rn(z[8 * j + 2 * e + 1]);
+                  const __half2 hh = __halves2half2(h0, h1);
+                  const __half2 ll = __floats2half2_rn(z[8 * j + 2 * e] - __half2float(h0),
+                                                       z[8 * j + 2 * e + 1] - __half2float(h1));
+                  hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
+                  lw[e] = *reinterpret_cast<const uint32_t*>(&ll);
+                }
+                const int off = ((p >> 3) * (RP / 8) + j) * 128 + (p & 7) * 16;
+                *reinterpret_cast<uint4*>(Zh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(Zl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+              }
+            }
+            prod_sync();
+          }
+        }
+        // ---- k_hat (hi, lo) of 64 keys: thread = (key, 32-channel group) ----
+        {
+          const int key = hk * 64 + (p >> 2), grp = p & 3;
+          const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
+          const uint2 kc = *reinterpret_cast<const uint2*>(tb + a.off.kcode + key * 32 + grp * 8);
+          const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.kqp + (key * G + grp) * 4);
           const float kz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
           const float ks = __half2float(__ushort_as_half((unsigned short)(qp >> 16)));
           const float2 kz2 = make_float2(kz, kz), ks2 = make_float2(ks, ks);
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {
-            const int chunk = half * 8 + gg * 4 + c8;          // 8-channel chunk 0..15
+            const int chunk = grp * 4 + c8;          // 8-channel chunk 0..15
             uint4 craw;
             if (CS) craw = *reinterpret_cast<const uint4*>(Cs + cswz(idx, chunk));
             else craw = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)idx * kD + 8 * chunk));
             const uint32_t cw[4] = {craw.x, craw.y, craw.z, craw.w};
-            const uint32_t bits = (kw[gg * 2 + (c8 >> 1)] >> (16 * (c8 & 1))) & 0xffffu;
+            const uint32_t bits = ((c8 >> 1) ? kc.y : kc.x) >> (16 * (c8 & 1)) & 0xffffu;
             uint32_t ph[4], pl[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
@@ -494,29 +530,31 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
             *reinterpret_cast<uint4*>(Khi + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
             *reinterpret_cast<uint4*>(Klo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
           }
-        }
-        if constexpr (RP > 0) {
-          if (half == 0) {
-            const __half* esrc = reinterpret_cast<const __half*>(tb + a.off.e) + key * a.r;
+          if constexpr (RP > 0) {
+            if (p < 64) {
+              const int ek = hk * 64 + p;
+              const __half* esrc = reinterpret_cast<const __half*>(tb + a.off.e) + ek * a.r;
 #pragma unroll
-            for (int j = 0; j < RP / 8; ++j) {
-              uint32_t w[4];
+              for (int j = 0; j < RP / 8; ++j) {
+                uint32_t w[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int m0 = 8 * j + 2 * e;
-                const __half e0 = m0 < a.r ? esrc[m0] : __float2half_rn(0.f);
-                const __half e1 = m0 + 1 < a.r ? esrc[m0 + 1] : __float2half_rn(0.f);
-                const __half2 ee = __halves2half2(e0, e1);
-                w[e] = *reinterpret_cast<const uint32_t*>(&ee);
+                for (int e = 0; e < 4; ++e) {
+                  const int m0 = 8 * j + 2 * e;
+                  const __half e0 = m0 < a.r ? esrc[m0] : __float2half_rn(0.f);
+                  const __half e1 = m0 + 1 < a.r ? esrc[m0 + 1] : __float2half_rn(0.f);
+                  const __half2 ee = __halves2half2(e0, e1);
+                  w[e] = *reinterpret_cast<const uint32_t*>(&ee);
+                }
+                *reinterpret_cast<uint4*>(Es + ((ek >> 3) * (RP / 8) + j) * 128 + (ek & 7) * 16) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
               }
-              *reinterpret_cast<uint4*>(Es + ((key >> 3) * (RP / 8) + j) * 128 + (key & 7) * 16) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
             }
           }
         }
+        fence_async_smem();
+        bar_arrive(hk == 0 ? kA_ready : kB_ready);
       }
-      fence_async_smem();
-      bar_arrive(k_ready);
+      if (!ok) break;
       // ---- v_hat^T ----
       if (t > 0) {
         if (!prod_all(bar_wait(pv_done, (uint32_t)((t - 1) & 1), &abort_sh, a.status))) { ok = false; break; }
@@ -561,53 +599,112 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     const bool leader = lane == 0;
     bool ok = true;
     const uint32_t kh = su32(Khi), kl = su32(Klo), vt = su32(Vt);
-    ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
-    fence_after();
     const uint32_t ea = su32(Es), za = su32(Zh), zl = su32(Zl);
     constexpr uint32_t kSbo = (RP / 8) * 128;
-    for (int64_t t = 0; t <= nt && ok; ++t) {
-      if (t < nt) {
-        const int b = (int)(t & 1);
-        if (!warp_all(bar_wait(k_ready, (uint32_t)(t & 1), &abort_sh, a.status))) { ok = false; break; }
-        if (t >= 2 && !warp_all(bar_wait(&s_free[b], (uint32_t)(((t >> 1) - 1) & 1), &abort_sh, a.status))) { ok = false; break; }
-        fence_after();
-        if (leader) {
-          const uint32_t d = tmem + kColS0 + 128u * b;
+    ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
+    fence_after();
+    // Issue whatever is ready, in tile order per stream: S(t) first half,
+    // S(t) second half, O += P(t) V(t).  Readiness is probed without
+    // blocking (lane 0 probes, the warp follows its answer).
+    int64_t nA = 0, nB = 0, nP = 0;
+    long long last = clock64();
+    while (ok && nP < nt) {
+      bool did = false;
+      if (nA < nt && nA == nB) {
+        const int b = (int)(nA & 1);
+        bool rdy = false;
+        if (leader) rdy = bar_test(kA_ready, (uint32_t)(nA & 1)) &&
+                          (nA < 2 || bar_test(&s_free[b], (uint32_t)(((nA >> 1) - 1) & 1)));
+        if (__shfl_sync(0xffffffffu, rdy, 0)) {
+          fence_after();
+          if (leader) {
+            const uint32_t d = tmem + kColS0 + 128u * b;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-            mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kh + ko), kIdescQK, j > 0);
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-            mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kl + ko), kIdescQK, 1);
-          }
-          if constexpr (RP > 0) {
-#pragma unroll
-            for (int kk = 0; kk < RP / 16; ++kk) {
-              mma_ss(d, desc_none(za + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
-              mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kh + ko), kIdescQK64, j > 0);
             }
-          }
-          commit(&s_done[b]);
-        }
-        __syncwarp();
-      }
-      if (t >= 1) {
-        const int64_t u = t - 1;
-        if (!warp_all(bar_wait(p_ready, (uint32_t)(u & 1), &abort_sh, a.status))) { ok = false; break; }
-        if (!warp_all(bar_wait(v_ready, (uint32_t)(u & 1), &abort_sh, a.status))) { ok = false; break; }
-        fence_after();
-        if (leader) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            mma_ts(tmem + kColO, tmem + kColP + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV, (u > 0 || j > 0) ? 1u : 0u);
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kl + ko), kIdescQK64, 1);
+            }
+            if constexpr (RP > 0) {
+#pragma unroll
+              for (int kk = 0; kk < RP / 16; ++kk) {
+                mma_ss(d, desc_none(za + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16_64, 1);
+                mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16_64, 1);
+              }
+            }
+            commit(&sA_done[b]);
           }
-          commit(pv_done);
+          __syncwarp();
+          ++nA;
+          did = true;
         }
-        __syncwarp();
       }
+      if (nB < nA) {
+        const int b = (int)(nB & 1);
+        bool rdy = false;
+        if (leader) rdy = bar_test(kB_ready, (uint32_t)(nB & 1));
+        if (__shfl_sync(0xffffffffu, rdy, 0)) {
+          fence_after();
+          if (leader) {
+            const uint32_t d = tmem + kColS0 + 128u * b + 64;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32 + 8192;   // key rows 64..127
+              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kh + ko), kIdescQK64, j > 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32 + 8192;
+              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kl + ko), kIdescQK64, 1);
+            }
+            if constexpr (RP > 0) {
+#pragma unroll
+              for (int kk = 0; kk < RP / 16; ++kk) {
+                const uint32_t eb = ea + 8 * kSbo + 256 * kk;
+                mma_ss(d, desc_none(za + 256 * kk, 128, kSbo), desc_none(eb, 128, kSbo), kIdescF16_64, 1);
+                mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(eb, 128, kSbo), kIdescF16_64, 1);
+              }
+            }
+            commit(&sB_done[b]);
+          }
+          __syncwarp();
+          ++nB;
+          did = true;
+        }
+      }
+      if (nP < nB) {
+        bool rdy = false;
+        if (leader) rdy = bar_test(p_ready, (uint32_t)(nP & 1)) && bar_test(v_ready, (uint32_t)(nP & 1));
+        if (__shfl_sync(0xffffffffu, rdy, 0)) {
+          fence_after();
+          if (leader) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              mma_ts(tmem + kColO, tmem + kColP + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
+                     (nP > 0 || j > 0) ? 1u : 0u);
+            commit(pv_done);
+          }
+          __syncwarp();
+          ++nP;
+          did = true;
+        }
+      }
+      if (did) {
+        last = clock64();
+      } else if (abort_sh) {
+        ok = false;
+      } else if (clock64() - last > kWaitCycles) {
+        if (leader) {
+          abort_sh = 1;
+          atomicOr(a.status, kDevTimeout);
+        }
+        ok = false;
+      }
+      ok = warp_all(ok);
     }
     // wait for the last PV before the TMEM can be released (bounded)
     if (ok && nt > 0) bar_wait(pv_done, (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
