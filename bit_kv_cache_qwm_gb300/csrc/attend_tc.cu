@@ -21,12 +21,10 @@
 //               into a no-swizzle K-major fp16 tile; recompute Z = q U_t^T as
 //               two fp16 terms when the tile's basis slot changes.
 //   warp 12     MMA issuer (one lane) and TMEM owner:
-//               S[t&1]  = Q khi^T + Q klo^T + Zhi E^T + Zlo E^T   (M=128)
-//               in two halves of 64 keys (N=64 each), so the producers
-//               dequantise one half while the tensor core multiplies the
-//               other, and O += P V_hat (A = P in TMEM).  The issuer probes
-//               the ready barriers without blocking and issues whatever is
-//               ready, in order within each stream.
+//               S[t&1]  = Q khi^T + Q klo^T + Zhi E^T + Zlo E^T   (M=N=128)
+//               and O += P V_hat (A = P in TMEM).  The issuer probes the
+//               ready barriers without blocking and issues whatever is ready,
+//               in order within each stream (S of a tile before its PV).
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384), P [384,448),
 // Q [448,512) (bf16 pairs).
 // Synchronisation: mbarriers (kA_ready, kB_ready, v_ready, p_ready, s_free[2],
@@ -182,6 +180,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Two 2-bit codes (bits 0-1 and 2-3 of n) as exact floats: 2^23 + c has c in
+// the low mantissa bits, so (2^23 | c) - 2^23 = c with no rounding.
+__device__ __forceinline__ float2 codes_f2(uint32_t n) {
+  const float2 m = make_float2(__uint_as_float(0x4B000000u | (n & 3u)), __uint_as_float(0x4B000000u | ((n >> 2) & 3u)));
+  return __fadd2_rn(m, make_float2(-8388608.f, -8388608.f));
+}
+// The same for fp16 pairs: 1024 + c is exact in fp16 (0x6400 | c).
+__device__ __forceinline__ __half2 codes_h2(uint32_t n) {
+  const uint32_t w = 0x64006400u | (n & 3u) | (((n >> 2) & 3u) << 16);
+  return __hsub2(*reinterpret_cast<const __half2*>(&w), __float2half2_rn(1024.f));
+}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -248,8 +257,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   uint8_t* Cs = Ring + 2 * a.off.bytes;  // C x 256 B (CS only)
   __shared__ __align__(8) uint64_t bars[14];
   __shared__ uint32_t tmem_base_sh;
-  __shared__ float2 code_f2[16];      // (c0, c1) of a 4-bit pair of 2-bit codes
-  __shared__ __half2 code_h2[16];
   __shared__ volatile int abort_sh;
   uint64_t* kA_ready = &bars[0];  // keys 0-63 of k_hat (and their e) written
   uint64_t* kB_ready = &bars[1];  // keys 64-127
@@ -267,10 +274,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   const int64_t row0 = (int64_t)blockIdx.x * 128;
   const int64_t nt = a.n_tiles;
 
-  if (tid < 16) {
-    code_f2[tid] = make_float2((float)(tid & 3), (float)(tid >> 2));
-    code_h2[tid] = __floats2half2_rn((float)(tid & 3), (float)(tid >> 2));
-  }
   if (tid == 0) {
     abort_sh = 0;
     bar_init(kA_ready, kProdThreads);
@@ -506,16 +509,19 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
           const float2 kz2 = make_float2(kz, kz), ks2 = make_float2(ks, ks);
 #pragma unroll
           for (int c8 = 0; c8 < 4; ++c8) {
-            const int chunk = grp * 4 + c8;          // 8-channel chunk 0..15
+            // chunk order rotated by the group: the 8 lanes of a store phase
+            // (2 keys x 4 groups) then hit 8 different bank groups
+            const int cl = (c8 + grp) & 3;
+            const int chunk = grp * 4 + cl;          // 8-channel chunk 0..15
             uint4 craw;
             if (CS) craw = *reinterpret_cast<const uint4*>(Cs + cswz(idx, chunk));
             else craw = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)idx * kD + 8 * chunk));
             const uint32_t cw[4] = {craw.x, craw.y, craw.z, craw.w};
-            const uint32_t bits = ((c8 >> 1) ? kc.y : kc.x) >> (16 * (c8 & 1)) & 0xffffu;
+            const uint32_t bits = ((cl >> 1) ? kc.y : kc.x) >> (16 * (cl & 1)) & 0xffffu;
             uint32_t ph[4], pl[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
-              const float2 cd = code_f2[(bits >> (4 * e2)) & 15u];
+              const float2 cd = codes_f2(bits >> (4 * e2));
               const float2 rq = __ffma2_rn(cd, ks2, kz2);                      // zero + code*scale
               const float2 cc = make_float2(__uint_as_float(cw[e2] << 16), __uint_as_float(cw[e2] & 0xffff0000u));
               const float2 kv = __fadd2_rn(cc, rq);                            // + centroid
@@ -578,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
             uint32_t w[4];
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
-              const __half2 hh = __hfma2(code_h2[(bits >> (4 * e2)) & 15u], vs2, vz2);   // zero + code*scale
+              const __half2 hh = __hfma2(codes_h2(bits >> (4 * e2)), vs2, vz2);   // zero + code*scale
               w[e2] = *reinterpret_cast<const uint32_t*>(&hh);
             }
             *reinterpret_cast<uint4*>(Vt + sw128_off(key, chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -610,68 +616,38 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     long long last = clock64();
     while (ok && nP < nt) {
       bool did = false;
-      if (nA < nt && nA == nB) {
+      if (nA < nt) {
         const int b = (int)(nA & 1);
         bool rdy = false;
-        if (leader) rdy = bar_test(kA_ready, (uint32_t)(nA & 1)) &&
+        if (leader) rdy = bar_test(kA_ready, (uint32_t)(nA & 1)) && bar_test(kB_ready, (uint32_t)(nA & 1)) &&
                           (nA < 2 || bar_test(&s_free[b], (uint32_t)(((nA >> 1) - 1) & 1)));
         if (__shfl_sync(0xffffffffu, rdy, 0)) {
           fence_after();
           if (leader) {
+            // full N = 128 MMAs: N = 64 halves run at a fraction of the rate
             const uint32_t d = tmem + kColS0 + 128u * b;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kh + ko), kIdescQK64, j > 0);
+              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kh + ko), kIdescQK, j > 0);
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kl + ko), kIdescQK64, 1);
+              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kl + ko), kIdescQK, 1);
             }
             if constexpr (RP > 0) {
 #pragma unroll
               for (int kk = 0; kk < RP / 16; ++kk) {
-                mma_ss(d, desc_none(za + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16_64, 1);
-                mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16_64, 1);
+                mma_ss(d, desc_none(za + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
+                mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
               }
             }
             commit(&sA_done[b]);
-          }
-          __syncwarp();
-          ++nA;
-          did = true;
-        }
-      }
-      if (nB < nA) {
-        const int b = (int)(nB & 1);
-        bool rdy = false;
-        if (leader) rdy = bar_test(kB_ready, (uint32_t)(nB & 1));
-        if (__shfl_sync(0xffffffffu, rdy, 0)) {
-          fence_after();
-          if (leader) {
-            const uint32_t d = tmem + kColS0 + 128u * b + 64;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32 + 8192;   // key rows 64..127
-              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kh + ko), kIdescQK64, j > 0);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32 + 8192;
-              mma_ts(d, tmem + kColQ + 8 * j, desc_sw128(kl + ko), kIdescQK64, 1);
-            }
-            if constexpr (RP > 0) {
-#pragma unroll
-              for (int kk = 0; kk < RP / 16; ++kk) {
-                const uint32_t eb = ea + 8 * kSbo + 256 * kk;
-                mma_ss(d, desc_none(za + 256 * kk, 128, kSbo), desc_none(eb, 128, kSbo), kIdescF16_64, 1);
-                mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(eb, 128, kSbo), kIdescF16_64, 1);
-              }
-            }
             commit(&sB_done[b]);
           }
           __syncwarp();
+          ++nA;
           ++nB;
           did = true;
         }
