@@ -142,13 +142,15 @@ qwm_status qwm_calibrate(qwm_ctx* ctx, const void* d_q_hist, int64_t n_h, void* 
  * computes the same sensitivity s [H][d], basis U [H][r][d], eigenvalues
  * lambda [H][r] and energy [H] as qwm_calibrate (all float32, caller-owned
  * device buffers; U and lambda may be NULL when rank is 0) from q_hist
- * [H][n_h][d] (dtype QWM_F32 or QWM_BF16), with the Gram partial sums in one
- * 8 MiB array compiled into the library, which every GPU that loads the
- * library keeps until the process exits.
- *   - Limit: the partial sums of at least one split, H*d*d floats (plus the
- *     eigen-solver's spill when rank + oversample > 44 at d = 128), must fit in
- *     8 MiB; larger requests return QWM_ERR_CAPACITY before any launch.  With
- *     d = 128 that is up to 127 heads.
+ * [H][n_h][d] (dtype QWM_F32 or QWM_BF16), with its scratch (Gram partial
+ * sums, A^2, eigen-solver buffers) in one 8 MiB array compiled into the
+ * library, which every GPU that loads the library keeps until the process
+ * exits.
+ *   - Limit: one split of partial sums (H*d*d floats) plus A^2 (H*d*d floats)
+ *     must fit in 8 MiB; when rank + oversample > 64 the whole-matrix solver
+ *     needs no A^2 but spills 6*d*(d+1) floats per head at d = 128.  Larger
+ *     requests return QWM_ERR_CAPACITY before any launch.  That is up to 63
+ *     heads at d = 128 (18 when rank + oversample > 64) and 255 at d = 64.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) once for that device; make that first call before
  *     any stream capture.  No call allocates or frees memory.

@@ -56,7 +56,12 @@ def test_static_calibration_matches_context_calibration(qwm, name, dtype, r):
 
 
 def test_static_calibration_rejects_oversized_requests(qwm):
-    q = torch.zeros((128, 8, 128), dtype=torch.bfloat16, device="cuda")
+    """At d = 128 one split of partial sums plus A^2 is 128 KiB per head: 63
+    heads fit in the 8 MiB array, 64 do not (rejected before any launch)."""
+    q = torch.zeros((64, 8, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(qwm.QwmError) as e:
         qwm.qwm_calibrate_static(q, 16)
     assert e.value.status == 3
+    out = qwm.qwm_calibrate_static(q[:63], 16)
+    torch.cuda.synchronize()
+    assert (out["s"] == 0).all() and torch.isfinite(out["U"]).all()
