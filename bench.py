@@ -230,7 +230,7 @@ def run_gpu(args):
     # the centroids: 25 Lloyd iterations on the keys of frame 0, on the GPU
     cent = qwm.qwm_kmeans(T(kf), torch.from_numpy(rows).to(dev), C, iters=25)
     ctx.set_centroids(cent)
-    ctx.set_attend_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3}[args.kernel])
+    ctx.set_attend_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4}[args.kernel])
     qh = T(synth.hist_queries(wl, 0))
     ctx.calibrate(qh)
     for ch in range(n_prefix):
@@ -333,7 +333,7 @@ def run_gpu(args):
     att_ms = float(np.mean(att))
     achieved = flops / (att_ms * 1e-3) / 1e12
     value = whole_job_tflops(flops, world, ms_step)
-    kernel = {0: "auto", 1: "simt", 2: "mma", 3: "tcgen05"}
+    kernel = {0: "auto", 1: "simt", 2: "mma", 3: "tcgen05", 4: "tcgen05-2tile"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -381,7 +381,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", choices=["", "attend", "append", "calibrate"],
                     help="profiling mode: set up the workload, then run only this call --steps times")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma", "tc"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma", "tc", "tc2"],
                     help="attention kernel (auto picks the fastest that applies)")
     args = ap.parse_args()
     if args.impl == "reference":

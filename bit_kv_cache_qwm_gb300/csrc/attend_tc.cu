@@ -50,9 +50,6 @@ constexpr uint32_t kDevTimeout = 0x4u;
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | (16u << 17) | (8u << 24);  // bf16 x bf16 -> f32
 constexpr uint32_t kIdescF16 = (1u << 4) | (16u << 17) | (8u << 24);                           // f16 x f16 -> f32
 constexpr uint32_t kIdescPV = kIdescF16 | (1u << 16);                                          // B MN-major
-// N = 64 halves of the S tile
-constexpr uint32_t kIdescQK64 = (1u << 4) | (1u << 7) | (1u << 10) | (8u << 17) | (8u << 24);
-constexpr uint32_t kIdescF16_64 = (1u << 4) | (8u << 17) | (8u << 24);
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -167,14 +164,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
                  "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]),
                  "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
                  "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-               "%14,%15,%16};"
-               ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
-                 "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]),
-                 "r"(v[14]), "r"(v[15])
                : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -692,6 +681,557 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
   if (warp == 12) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
+
+// ---------------------------------------------------------------------------
+// Two query tiles per CTA.  The k_hat, e and v_hat tiles a CTA dequantises
+// feed two M = 128 MMAs (query rows 0-127 and 128-255 of the CTA), which
+// halves the dequantisation per flop.  Warp roles:
+//   warps 0-3 / 4-7  softmax of query tile a / b (thread = row; TMEM lane =
+//                    row).  Load their Q rows into shared memory once (the
+//                    A operand of QK^T), online softmax as in the one-tile
+//                    kernel, P (fp16) written over the first 64 columns of
+//                    their own S buffer.
+//   warps 8-14       producers: k_hat (hi, lo), e, v_hat and Z = q U_t^T for
+//                    both query tiles; centroids read through L2.
+//   warp 15          MMA issuer and TMEM owner: S_g(t) = Q_g khi^T + Q_g
+//                    klo^T + Zhi_g E^T + Zlo_g E^T, O_g += P_g V_hat, for
+//                    g = a, b; S_g(t+1) is issued after PV_g(t), so the
+//                    tensor pipe's in-order execution keeps P_g(t) intact
+//                    until PV_g(t) has read it.
+// TMEM columns: S_a [0,128), S_b [128,256), O_a [256,384), O_b [384,512).
+// Split KV: with gridDim.z = 2 the two CTAs of a cluster take the two halves
+// of the tile range for the same query rows; rank 1 sends its unnormalised
+// O, running maximum and sum to rank 0 through distributed shared memory
+// (into buffers rank 0 no longer needs) and rank 0 merges them:
+// m = max(m0, m1), O = (O0 2^(m0-m) + O1 2^(m1-m)) / (l0 2^(m0-m) + l1 2^(m1-m)).
+// 16 warps: 4 per SM sub-partition, which leaves 128 registers a thread
+constexpr int kSoft2Warps = 8, kProd2Warps = 7;
+constexpr int kThreads2 = (kSoft2Warps + kProd2Warps + 1) * 32;   // 512
+constexpr int kMmaWarp2 = kSoft2Warps + kProd2Warps;             // 15
+constexpr uint32_t kColOa = 256;
+
+__device__ __forceinline__ void prod2_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kProd2Warps * 32) : "memory"); }
+__device__ __forceinline__ bool prod2_all(bool v) {
+  uint32_t r;
+  asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, %2, p;\n"
+               "selp.u32 %0, 1, 0, q;\n}"
+               : "=r"(r) : "r"((uint32_t)v), "n"(kProd2Warps * 32) : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared-memory address of the same location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+constexpr int kRecvLd = 132;   // floats per row of a received partial: O[128], m, l, ok, pad
+
+template <int RP>
+__global__ void __launch_bounds__(kThreads2, 1) attend_tc2_kernel(const TcArgs a) {
+  constexpr int G = kD / kGroup;
+  constexpr int kZBytes = 128 * RP * 2;
+  extern __shared__ __align__(1024) uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((1024 - (su32(sm_raw) & 1023)) & 1023);
+  uint8_t* Qs = sm;                       // 2 x 32 KB: Q_a, Q_b (SW128 K-major)
+  uint8_t* Khi = sm + 65536;              // 32 KB
+  uint8_t* Klo = sm + 98304;              // 32 KB
+  uint8_t* Vt = sm + 131072;              // 32 KB
+  uint8_t* Es = sm + 163840;              // 128 x RP fp16, core matrices
+  uint8_t* Zs = Es + kZBytes;             // [tile g][hi, lo] 128 x RP fp16
+  uint8_t* Ring = Zs + 4 * kZBytes;       // 2 x tile bytes (packed tiles)
+  __shared__ __align__(8) uint64_t bars[11];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ volatile int abort_sh;
+  uint64_t* k_ready = &bars[0];   // k_hat, e (and Z) of tile t written
+  uint64_t* v_ready = &bars[1];
+  uint64_t* s_done = &bars[2];    // [2] S_g(t) computed
+  uint64_t* p_ready = &bars[4];   // [2] P_g(t) written
+  uint64_t* pv_done = &bars[6];   // [2] O_g += P_g(t) V(t) done
+  uint64_t* full = &bars[8];      // [2] packed tile landed in ring stage
+  uint64_t* q_ready = &bars[10];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y;
+  const int64_t row0 = (int64_t)blockIdx.x * 256;
+  // this CTA's share of the tile range (split KV across the cluster)
+  const int nsplit = (int)gridDim.z;
+  const int split = nsplit > 1 ? (int)cluster_rank() : 0;
+  const int64_t t_begin = a.n_tiles * split / nsplit;
+  const int64_t nt = a.n_tiles * (split + 1) / nsplit - t_begin;
+  constexpr int kProdThreads2 = kProd2Warps * 32;
+  float m_run = -INFINITY, l_run = 0.f;   // softmax row state, used by the epilogue
+  bool sm_ok = false;
+
+  if (tid == 0) {
+    abort_sh = 0;
+    bar_init(k_ready, kProdThreads2);
+    bar_init(v_ready, kProdThreads2);
+    for (int g = 0; g < 2; ++g) {
+      bar_init(&s_done[g], 1);
+      bar_init(&p_ready[g], 128);
+      bar_init(&pv_done[g], 1);
+      bar_init(&full[g], 1);
+    }
+    bar_init(q_ready, 256);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kMmaWarp2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(su32(&tmem_base_sh)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (warp < kSoft2Warps) {
+    // ------------------------------------------------------------ softmax
+    const int g = warp >> 2, i = tid & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t colS = 128u * g, colO = kColOa + 128u * g;
+    const float c2 = a.scale_log2;
+    bool ok = true;
+    const int64_t grow = row0 + 128 * g + i;
+    {
+      // this thread's Q row into the SW128 K-major A tile of query tile g
+      const uint4* src = reinterpret_cast<const uint4*>(a.Q + ((int64_t)h * a.M + grow) * kD);
+      uint8_t* qt = Qs + g * 32768;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 x = grow < a.M ? src[c] : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qt + sw128_off(i, c)) = x;
+      }
+      fence_async_smem();
+      bar_arrive(q_ready);
+    }
+    for (int64_t t = 0; t < nt && ok; ++t) {
+      const int nv = a.tiles[t_begin + t].y;
+      if (!warp_all(bar_wait(&s_done[g], (uint32_t)(t & 1), &abort_sh, a.status))) { ok = false; break; }
+      fence_after();
+      const uint32_t sbase = tmem + lane_base + colS;
+      float mx = -INFINITY;
+      const bool ragged = nv < 128;
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t v[64];
+        tmem_ld64(sbase + 64 * cb, v);
+        tmem_wait_ld();
+        if (!ragged) {
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) mx = max3f(mx, __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k)
+            if (64 * cb + k < nv) mx = fmaxf(mx, __uint_as_float(v[k]));
+        }
+      }
+      const float mnew = fmaxf(m_run, mx * c2);
+      // PV_g(t-1) has read P_g(t-1) and finished O_g before either changes
+      if (t > 0) {
+        if (!warp_all(bar_wait(&pv_done[g], (uint32_t)((t - 1) & 1), &abort_sh, a.status))) { ok = false; break; }
+        fence_after();
+      }
+      const bool need = mnew > m_run + 8.f;
+      if (t > 0 && __any_sync(0xffffffffu, need)) {
+        const float corr = need ? ex2(m_run - mnew) : 1.f;
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + colO + 32 * cb, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * corr);
+          tmem_st32(tmem + lane_base + colO + 32 * cb, v);
+        }
+        l_run *= corr;
+      }
+      if (need) m_run = mnew;
+      float2 psum2 = make_float2(0.f, 0.f);
+      const float2 c2v = make_float2(c2, c2), mv = make_float2(-m_run, -m_run);
+      for (int cb = 0; cb < 2; ++cb) {
+        uint32_t v[64], pk[32];
+        tmem_ld64(sbase + 64 * cb, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 arg = __ffma2_rn(make_float2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1])), c2v, mv);
+          float2 pp = make_float2(ex2(arg.x), ex2(arg.y));
+          if (ragged) {
+            const int k0 = 64 * cb + 2 * k;
+            pp.x = k0 < nv ? pp.x : 0.f;
+            pp.y = k0 + 1 < nv ? pp.y : 0.f;
+          }
+          psum2 = __fadd2_rn(psum2, pp);
+          const __half2 hp = __floats2half2_rn(pp.x, pp.y);
+          pk[k] = *reinterpret_cast<const uint32_t*>(&hp);
+        }
+        // P over S columns already read (pair 32cb.. from columns 64cb..)
+        tmem_st32(sbase + 32 * cb, pk);
+      }
+      l_run += psum2.x + psum2.y;
+      tmem_wait_st();
+      fence_before();
+      bar_arrive(&p_ready[g]);
+    }
+    if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
+    fence_after();
+    sm_ok = ok;
+  } else if (warp < kMmaWarp2) {
+    // ------------------------------------------------------------ producers
+    const int p = tid - kSoft2Warps * 32;      // 0..223
+    const __nv_bfloat16* ch = a.cent + (int64_t)h * a.nC * kD;
+    int cur_slot = -1;
+    bool ok = true;
+    const uint32_t TB = (uint32_t)a.off.bytes;
+    const uint8_t* tiles_h = a.cache + (int64_t)h * a.max_tiles * a.off.bytes;
+    if (p == 0) {
+      for (int64_t u = 0; u < 2 && u < nt; ++u) {
+        bar_expect_tx(&full[u], TB);
+        bulk_g2s(Ring + u * TB, tiles_h + (t_begin + u) * TB, TB, &full[u]);
+      }
+    }
+    prod2_sync();
+    for (int64_t t = 0; t < nt && ok; ++t) {
+      const uint8_t* tb = Ring + (t & 1) * TB;
+      const int slot = a.tiles[t_begin + t].x;
+      if (!prod2_all(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
+      // S_a(t-1) and S_b(t-1) have read k_hat, e and Z
+      if (t > 0) {
+        const uint32_t par = (uint32_t)((t - 1) & 1);
+        if (!prod2_all(bar_wait(&s_done[0], par, &abort_sh, a.status) &&
+                       bar_wait(&s_done[1], par, &abort_sh, a.status))) { ok = false; break; }
+      }
+      if constexpr (RP > 0) {
+        if (slot != cur_slot) {
+          cur_slot = slot;
+          // stage U (fp32 [r][128]) in the free khi buffer, then Z = q U^T
+          // for the CTA's 256 query rows (thread = row)
+          float* Us = reinterpret_cast<float*>(Khi);
+          const float* U = a.basis + ((int64_t)slot * a.H + h) * a.r * kD;
+          for (int k = p; k < RP * kD; k += kProdThreads2) Us[k] = (k / kD) < a.r ? U[k] : 0.f;
+          prod2_sync();
+          for (int zr = p; zr < 256; zr += kProdThreads2) {
+          float z[RP];
+#pragma unroll
+          for (int k = 0; k < RP; ++k) z[k] = 0.f;
+          const int64_t grow = row0 + zr;
+          const uint4* qrow = reinterpret_cast<const uint4*>(a.Q + ((int64_t)h * a.M + grow) * kD);
+          for (int c8 = 0; c8 < 16; ++c8) {
+            const uint4 qv = grow < a.M ? qrow[c8] : make_uint4(0, 0, 0, 0);
+            const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float qf = __uint_as_float(e & 1 ? (qw[e >> 1] & 0xffff0000u) : (qw[e >> 1] << 16));
+              const int c = 8 * c8 + e;
+#pragma unroll
+              for (int k = 0; k < RP; ++k) z[k] = fmaf(qf, Us[k * kD + c], z[k]);
+            }
+          }
+          const int gq = zr >> 7, iq = zr & 127;
+          uint8_t* zh = Zs + (2 * gq) * kZBytes;
+          uint8_t* zl = zh + kZBytes;
+#pragma unroll
+          for (int j = 0; j < RP / 8; ++j) {
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __half h0 = __float2half_rn(z[8 * j + 2 * e]), h1 = __float2half_rn(z[8 * j + 2 * e + 1]);
+              const __half2 hh = __halves2half2(h0, h1);
+              const __half2 ll = __floats2half2_rn(z[8 * j + 2 * e] - __half2float(h0),
+                                                   z[8 * j + 2 * e + 1] - __half2float(h1));
+              hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
+              lw[e] = *reinterpret_cast<const uint32_t*>(&ll);
+            }
+            const int off = ((iq >> 3) * (RP / 8) + j) * 128 + (iq & 7) * 16;
+            *reinterpret_cast<uint4*>(zh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(zl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+          }
+          prod2_sync();
+        }
+      }
+      // ---- k_hat (hi, lo): item = (key, 32-channel group) ----
+#pragma unroll 1
+      for (int item = p; item < 512; item += kProdThreads2) {
+        const int key = item >> 2, grp = item & 3;
+        const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
+        const uint2 kc = *reinterpret_cast<const uint2*>(tb + a.off.kcode + key * 32 + grp * 8);
+        const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.kqp + (key * G + grp) * 4);
+        const float kz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
+        const float ks = __half2float(__ushort_as_half((unsigned short)(qp >> 16)));
+        const float2 kz2 = make_float2(kz, kz), ks2 = make_float2(ks, ks);
+        uint4 craw[4];
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          const int chunk = grp * 4 + ((c8 + grp) & 3);
+          craw[c8] = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)idx * kD + 8 * chunk));
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          // chunk order rotated by the group: the 8 lanes of a store phase
+          // (2 keys x 4 groups) then hit 8 different bank groups
+          const int cl = (c8 + grp) & 3;
+          const int chunk = grp * 4 + cl;
+          const uint32_t cw[4] = {craw[c8].x, craw[c8].y, craw[c8].z, craw[c8].w};
+          const uint32_t bits = ((cl >> 1) ? kc.y : kc.x) >> (16 * (cl & 1)) & 0xffffu;
+          uint32_t ph[4], pl[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float2 cd = codes_f2(bits >> (4 * e2));
+            const float2 rq = __ffma2_rn(cd, ks2, kz2);                      // zero + code*scale
+            const float2 cc = make_float2(__uint_as_float(cw[e2] << 16), __uint_as_float(cw[e2] & 0xffff0000u));
+            const float2 kv = __fadd2_rn(cc, rq);                            // + centroid
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(kv.x, kv.y);
+            const float2 hf = __bfloat1622float2(hb);
+            const float2 lo = __fadd2_rn(kv, make_float2(-hf.x, -hf.y));
+            const __nv_bfloat162 lb = __floats2bfloat162_rn(lo.x, lo.y);
+            ph[e2] = *reinterpret_cast<const uint32_t*>(&hb);
+            pl[e2] = *reinterpret_cast<const uint32_t*>(&lb);
+          }
+          const int off = sw128_off(key, chunk);
+          *reinterpret_cast<uint4*>(Khi + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          *reinterpret_cast<uint4*>(Klo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        }
+      }
+      if constexpr (RP > 0) {
+        if (p < 128) {
+          // e rows: thread = key
+          const __half* esrc = reinterpret_cast<const __half*>(tb + a.off.e) + p * a.r;
+#pragma unroll
+          for (int j = 0; j < RP / 8; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int m0 = 8 * j + 2 * e;
+              const __half e0 = m0 < a.r ? esrc[m0] : __float2half_rn(0.f);
+              const __half e1 = m0 + 1 < a.r ? esrc[m0 + 1] : __float2half_rn(0.f);
+              const __half2 ee = __halves2half2(e0, e1);
+              w[e] = *reinterpret_cast<const uint32_t*>(&ee);
+            }
+            *reinterpret_cast<uint4*>(Es + ((p >> 3) * (RP / 8) + j) * 128 + (p & 7) * 16) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      fence_async_smem();
+      bar_arrive(k_ready);
+      // ---- v_hat: PV_a(t-1) and PV_b(t-1) have read the previous one ----
+      if (t > 0) {
+        const uint32_t par = (uint32_t)((t - 1) & 1);
+        if (!prod2_all(bar_wait(&pv_done[0], par, &abort_sh, a.status) &&
+                       bar_wait(&pv_done[1], par, &abort_sh, a.status))) { ok = false; break; }
+      }
+      for (int item = p; item < 256; item += kProdThreads2) {
+        const int key = item & 127, half = item >> 7;
+        const uint4 vc = *reinterpret_cast<const uint4*>(tb + a.off.vcode + key * 32 + half * 16);
+        const uint2 vq = *reinterpret_cast<const uint2*>(tb + a.off.vqp + (key * G + 2 * half) * 4);
+        const uint32_t vw[4] = {vc.x, vc.y, vc.z, vc.w};
+#pragma unroll
+        for (int gg = 0; gg < 2; ++gg) {
+          const uint32_t qv = gg ? vq.y : vq.x;
+          const __half2 vz2 = __half2half2(__ushort_as_half((unsigned short)(qv & 0xffffu)));
+          const __half2 vs2 = __half2half2(__ushort_as_half((unsigned short)(qv >> 16)));
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            const int chunk = half * 8 + gg * 4 + c8;
+            const uint32_t bits = (vw[gg * 2 + (c8 >> 1)] >> (16 * (c8 & 1))) & 0xffffu;
+            uint32_t w[4];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+              const __half2 hh = __hfma2(codes_h2(bits >> (4 * e2)), vs2, vz2);   // zero + code*scale
+              w[e2] = *reinterpret_cast<const uint32_t*>(&hh);
+            }
+            *reinterpret_cast<uint4*>(Vt + sw128_off(key, chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      fence_async_smem();
+      bar_arrive(v_ready);
+      // every producer is done with ring stage t & 1: refill it with tile t + 2
+      prod2_sync();
+      if (p == 0 && t + 2 < nt) {
+        bar_expect_tx(&full[t & 1], TB);
+        bulk_g2s(Ring + (t & 1) * TB, tiles_h + (t_begin + t + 2) * TB, TB, &full[t & 1]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ MMA issuer
+    const bool leader = lane == 0;
+    bool ok = true;
+    const uint32_t qs = su32(Qs), kh = su32(Khi), kl = su32(Klo), vt = su32(Vt);
+    const uint32_t ea = su32(Es), zs = su32(Zs);
+    constexpr uint32_t kSbo = (RP / 8) * 128;
+    ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
+    fence_after();
+    // streams: S_a, S_b, PV_a, PV_b.  S_g(n) needs k_hat(n) and PV_g(n-1)
+    // issued; PV_g(n) needs S_g(n) issued, P_g(n) and v_hat(n).
+    int64_t nS[2] = {0, 0}, nP[2] = {0, 0};
+    long long last = clock64();
+    while (ok && (nP[0] < nt || nP[1] < nt)) {
+      bool did = false;
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int64_t n = nS[g];
+        if (n < nt && nP[g] == n) {
+          bool rdy = false;
+          if (leader) rdy = bar_test(k_ready, (uint32_t)(n & 1));
+          if (__shfl_sync(0xffffffffu, rdy, 0)) {
+            fence_after();
+            if (leader) {
+              const uint32_t d = tmem + 128u * g, qa = qs + 32768u * g;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+                mma_ss(d, desc_sw128(qa + ko), desc_sw128(kh + ko), kIdescQK, j > 0);
+              }
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+                mma_ss(d, desc_sw128(qa + ko), desc_sw128(kl + ko), kIdescQK, 1);
+              }
+              if constexpr (RP > 0) {
+                const uint32_t zh = zs + 2u * g * kZBytes, zl = zh + kZBytes;
+#pragma unroll
+                for (int kk = 0; kk < RP / 16; ++kk) {
+                  mma_ss(d, desc_none(zh + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
+                  mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
+                }
+              }
+              commit(&s_done[g]);
+            }
+            __syncwarp();
+            ++nS[g];
+            did = true;
+          }
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const int64_t n = nP[g];
+        if (n < nS[g]) {
+          bool rdy = false;
+          if (leader) rdy = bar_test(&p_ready[g], (uint32_t)(n & 1)) && bar_test(v_ready, (uint32_t)(n & 1));
+          if (__shfl_sync(0xffffffffu, rdy, 0)) {
+            fence_after();
+            if (leader) {
+              const uint32_t ps = tmem + 128u * g;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                mma_ts(tmem + kColOa + 128u * g, ps + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
+                       (n > 0 || j > 0) ? 1u : 0u);
+              commit(&pv_done[g]);
+            }
+            __syncwarp();
+            ++nP[g];
+            did = true;
+          }
+        }
+      }
+      if (did) {
+        last = clock64();
+      } else if (abort_sh) {
+        ok = false;
+      } else if (clock64() - last > kWaitCycles) {
+        if (leader) {
+          abort_sh = 1;
+          atomicOr(a.status, kDevTimeout);
+        }
+        ok = false;
+      }
+      ok = warp_all(ok);
+    }
+    // the last PVs complete before the TMEM is released (bounded)
+    if (ok && nt > 0) {
+      bar_wait(&pv_done[0], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+      bar_wait(&pv_done[1], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+    }
+  }
+
+  fence_before();
+  __syncthreads();
+  fence_after();
+  // ------------------------------------------------------------ epilogue
+  {
+    const int g = (warp >> 2) & 1, i = tid & 127;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t colO = kColOa + 128u * g;
+    const int64_t grow = row0 + 128 * g + i;
+    const bool softmax = warp < kSoft2Warps;
+    float* recv = reinterpret_cast<float*>(sm) + (128 * g + i) * kRecvLd;   // rank 0's buffers, now free
+    float f0 = 1.f, f1 = 0.f, inv = 0.f;
+    bool store = softmax && sm_ok;
+    if (nsplit > 1) {
+      cluster_sync();   // both CTAs are past their tiles
+      if (softmax && split == 1) {
+        const uint32_t dst = map_rank(su32(recv), 0);
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + colO + 32 * cb, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 8; ++q) st_cluster_v4(dst + (32 * cb + 4 * q) * 4, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+        st_cluster_v4(dst + 128 * 4, __float_as_uint(m_run), __float_as_uint(l_run), sm_ok ? 1u : 0u, 0u);
+      }
+      cluster_sync();   // the partials of rank 1 have landed
+      store = store && split == 0;
+      if (store) {
+        const float m1 = recv[128], l1 = recv[129];
+        store = __float_as_uint(recv[130]) != 0u;
+        const float mm = fmaxf(m_run, m1);
+        f0 = m_run == -INFINITY ? 0.f : ex2(m_run - mm);
+        f1 = m1 == -INFINITY ? 0.f : ex2(m1 - mm);
+        const float l = l_run * f0 + l1 * f1;
+        inv = l > 0.f ? 1.f / l : 0.f;
+      }
+    } else {
+      inv = l_run > 0.f ? 1.f / l_run : 0.f;
+    }
+    // every lane of a softmax warp loads (warp-collective); valid rows store
+    if (softmax && __any_sync(0xffffffffu, store)) {
+      __nv_bfloat16* dst = a.O + ((int64_t)h * a.M + grow) * kD;
+      for (int cb = 0; cb < 4; ++cb) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + colO + 32 * cb, v);
+        tmem_wait_ld();
+        if (store && grow < a.M) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 32 * cb + 8 * q + 2 * e;
+              float o0 = __uint_as_float(v[8 * q + 2 * e]) * f0, o1 = __uint_as_float(v[8 * q + 2 * e + 1]) * f0;
+              if (nsplit > 1) {
+                o0 = fmaf(recv[c], f1, o0);
+                o1 = fmaf(recv[c + 1], f1, o1);
+              }
+              const __nv_bfloat162 bb = __floats2bfloat162_rn(o0 * inv, o1 * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&bb);
+            }
+            *reinterpret_cast<uint4*>(dst + 32 * cb + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    }
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  if (warp == kMmaWarp2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+}
+
 size_t tc_smem(const qwm_ctx* c, int RP, bool cs) {
   return 1024 + 3 * 32768 + 3 * (size_t)128 * RP * 2 + 2 * c->lay.tile_bytes +
          (cs ? (size_t)c->cfg.n_centroids * 256 : 0);
@@ -708,14 +1248,48 @@ cudaError_t launch_rp(const qwm_ctx* c, const TcArgs& a, int64_t M, cudaStream_t
   return cudaGetLastError();
 }
 
-}  // namespace
-
-bool attend_tc_supported(const qwm_ctx* c) {
-  return c->cfg.dtype == QWM_BF16 && c->cfg.head_dim == kD && c->cfg.rank <= 32;
+size_t tc2_smem(const qwm_ctx* c, int RP) {
+  return 1024 + 5 * 32768 + 5 * (size_t)128 * RP * 2 + 2 * c->lay.tile_bytes;
 }
 
-cudaError_t launch_attend_tc(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
-                             cudaStream_t st) {
+// KV splits per query-row pair: 2 (a cluster of two CTAs) when that cuts
+// the number of full waves over the SMs, else 1
+int tc2_splits(const qwm_ctx* c, int64_t M) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    return 1;
+  const int64_t units = ((M + 255) / 256) * c->cfg.heads;
+  const int64_t w1 = (units + sms - 1) / sms;         // waves with one split
+  const int64_t w2x2 = (2 * units + sms - 1) / sms;   // twice the waves with two splits
+  return (c->n_tiles >= 2 && w2x2 < 2 * w1) ? 2 : 1;
+}
+
+template <int RP>
+cudaError_t launch_tc2(const qwm_ctx* c, const TcArgs& a, int64_t M, cudaStream_t st) {
+  const size_t smem = tc2_smem(c, RP);
+  auto kern = attend_tc2_kernel<RP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int ns = tc2_splits(c, M);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((M + 255) / 256), (unsigned)c->cfg.heads, (unsigned)ns);
+  cfg.blockDim = dim3(kThreads2, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)ns;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+TcArgs tc_args(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out) {
   TcArgs a;
   a.Q = (const __nv_bfloat16*)q;
   a.O = (__nv_bfloat16*)out;
@@ -733,11 +1307,34 @@ cudaError_t launch_attend_tc(const qwm_ctx* c, const void* q, int64_t M, float s
   a.r = c->cfg.rank;
   a.ib = c->ib;
   a.status = c->status;
+  return a;
+}
+
+}  // namespace
+
+bool attend_tc_supported(const qwm_ctx* c) {
+  return c->cfg.dtype == QWM_BF16 && c->cfg.head_dim == kD && c->cfg.rank <= 32;
+}
+
+bool attend_tc2_supported(const qwm_ctx* c) {
+  return c->cfg.dtype == QWM_BF16 && c->cfg.head_dim == kD && c->cfg.rank <= 16 &&
+         tc2_smem(c, c->cfg.rank == 0 ? 0 : 16) <= 227 * 1024;
+}
+
+cudaError_t launch_attend_tc(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                             cudaStream_t st) {
+  const TcArgs a = tc_args(c, q, M, scale, out);
   const int RP = a.r == 0 ? 0 : (a.r <= 16 ? 16 : 32);
   const bool cs = c->cfg.n_centroids <= 256;
   if (RP == 0) return cs ? launch_rp<0, true>(c, a, M, st) : launch_rp<0, false>(c, a, M, st);
   if (RP == 16) return cs ? launch_rp<16, true>(c, a, M, st) : launch_rp<16, false>(c, a, M, st);
   return cs ? launch_rp<32, true>(c, a, M, st) : launch_rp<32, false>(c, a, M, st);
+}
+
+cudaError_t launch_attend_tc2(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                              cudaStream_t st) {
+  const TcArgs a = tc_args(c, q, M, scale, out);
+  return a.r == 0 ? launch_tc2<0>(c, a, M, st) : launch_tc2<16>(c, a, M, st);
 }
 
 }  // namespace qwm

@@ -251,7 +251,9 @@ extern "C" qwm_status qwm_attend(qwm_ctx* x, const void* d_q, int64_t M, float s
   int k = qwm_resolved_attend_kernel(x);
   if (k == 2 && !attend_mma_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 3 && !attend_tc_supported(x)) return QWM_ERR_UNSUPPORTED;
-  cudaError_t e = k == 3   ? launch_attend_tc(x, d_q, M, scale, d_out, S(stream))
+  if (k == 4 && !attend_tc2_supported(x)) return QWM_ERR_UNSUPPORTED;
+  cudaError_t e = k == 4   ? launch_attend_tc2(x, d_q, M, scale, d_out, S(stream))
+                  : k == 3 ? launch_attend_tc(x, d_q, M, scale, d_out, S(stream))
                   : k == 2 ? launch_attend_mma(x, d_q, M, scale, d_out, S(stream))
                            : launch_attend_simt(x, d_q, M, scale, d_out, S(stream));
   return cuda_status(e);
@@ -291,7 +293,7 @@ extern "C" qwm_status qwm_get_status(qwm_ctx* x, void* stream) {
 }
 
 extern "C" qwm_status qwm_set_attend_kernel(qwm_ctx* x, int32_t k) {
-  if (!x || k < 0 || k > 3) return QWM_ERR_INVALID_ARG;
+  if (!x || k < 0 || k > 4) return QWM_ERR_INVALID_ARG;
   x->attend_kernel = k;
   return QWM_OK;
 }
@@ -299,6 +301,7 @@ extern "C" qwm_status qwm_set_attend_kernel(qwm_ctx* x, int32_t k) {
 extern "C" int32_t qwm_resolved_attend_kernel(const qwm_ctx* x) {
   if (!x) return -1;
   if (x->attend_kernel != 0) return x->attend_kernel;
+  if (attend_tc2_supported(x)) return 4;
   if (attend_tc_supported(x)) return 3;
   return attend_mma_supported(x) ? 2 : 1;
 }

@@ -71,6 +71,9 @@ bool attend_mma_supported(const qwm_ctx* c);
 cudaError_t launch_attend_tc(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
                              cudaStream_t st);
 bool attend_tc_supported(const qwm_ctx* c);
+bool attend_tc2_supported(const qwm_ctx* c);
+cudaError_t launch_attend_tc2(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                              cudaStream_t st);
 size_t gram_workspace_bytes(const qwm_config& cfg);
 
 // ---- device helpers ----

@@ -222,12 +222,15 @@ qwm_status qwm_kmeans(int32_t heads, int32_t head_dim, int32_t dtype, int32_t n_
                       const void* d_keys, int64_t n, const int32_t* d_init_rows, int32_t iters,
                       void* d_centroids, void* d_workspace, void* stream);
 
-/* Attention kernel choice: 0 = automatic (the tcgen05 kernel for bf16,
- * d = 128, r <= 32; else the CUDA-core kernel), 1 = float32 CUDA-core kernel,
- * 2 = bf16 mma.sync kernel, 3 = bf16 tcgen05 kernel. */
+/* Attention kernel choice: 0 = automatic (bf16 and d = 128: kernel 4 when
+ * r <= 16, kernel 3 when r <= 32; otherwise kernel 2 where it applies, else
+ * kernel 1), 1 = float32 CUDA-core kernel, 2 = bf16 mma.sync kernel, 3 = bf16
+ * tcgen05 kernel with 128 query rows per CTA, 4 = bf16 tcgen05 kernel with 256
+ * query rows per CTA (r <= 16).  An explicit choice the configuration does not
+ * support makes qwm_attend return QWM_ERR_UNSUPPORTED. */
 qwm_status qwm_set_attend_kernel(qwm_ctx* ctx, int32_t kernel);
 
-/* The attention kernel qwm_attend will run (1, 2 or 3; automatic resolved). */
+/* The attention kernel qwm_attend will run (1 to 4; automatic resolved). */
 int32_t qwm_resolved_attend_kernel(const qwm_ctx* ctx);
 
 int64_t qwm_num_tokens(const qwm_ctx* ctx);    /* valid tokens cached        */

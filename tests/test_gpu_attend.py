@@ -117,7 +117,7 @@ def test_full_rank_compensation_on_gpu(qwm, kernel):
     assert np.abs(got - want).max() <= 1e-5 * vmax
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 def test_attend_bf16_sampled_rows(qwm, kernel):
     """12 heads over 3 appends; the oracle checks every row of heads 0 and 9."""
     name = "bf16-h12-n32760"
@@ -129,7 +129,7 @@ def test_attend_bf16_sampled_rows(qwm, kernel):
     assert np.abs(got[[0, 9]] - want).max() <= 1e-2 * vmax
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("name,C,r", [("bf16-h12-n32760", 256, 16), ("bf16-h24-append-sweep", 1024, 32),
                                       ("bf16-h24-append-sweep", 64, 8), ("bf16-h24-append-sweep", 256, 0),
                                       ("bf16-h40-n98280-outlier", 256, 16)])
@@ -152,6 +152,12 @@ def test_attend_bf16_variants(qwm, kernel, name, C, r):
             ctx.set_calibration(s_, U)
             bases.append(U)
         ctx.append(_tensor(synth.keys(wl, ch, heads, n), "bf16"), _tensor(synth.values(wl, ch, heads, n), "bf16"))
+    if kernel == 4 and r > 16:
+        ctx.set_attend_kernel(kernel)
+        with pytest.raises(qwm.QwmError) as e:
+            ctx.attend(_tensor(synth.queries(wl, 3, heads, m=8), "bf16"))
+        assert e.value.status == 2                 # unsupported: r > 16
+        return
     ctx.set_attend_kernel(kernel)
     q = synth.queries(wl, 3, heads, m=200)
     got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
@@ -169,10 +175,26 @@ def test_attend_full_size_bench_configuration(qwm):
     wl, ctx, cent, bases = _build(qwm, name, list(range(12)), [wl_chunk for wl_chunk in [4680] * 7])
     q = synth.queries(wl, 0)
     got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
-    assert ctx.resolved_attend_kernel == 3
+    assert ctx.resolved_attend_kernel == 4
     rows = np.sort(np.random.default_rng(5).choice(wl.n_query, 48, replace=False))
     qs = q[:, rows]
     want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, qs, [0, 11], 1 / np.sqrt(128))
     err = np.abs(got[[0, 11]][:, rows] - want).max()
     assert err <= 1e-2 * vmax, (err, vmax)
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("sizes", [[100], [128, 5], [300, 1, 228]])
+def test_attend_two_tile_kernel_split_boundaries(qwm, sizes):
+    """Kernel 4 (256 query rows per CTA) on a cache of one tile (no KV split),
+    two tiles (one tile per split) and five tiles (an odd count split 2 + 3),
+    with M = 300 (two row blocks, the second ragged)."""
+    name = "bf16-h12-n32760"
+    wl, ctx, cent, bases = _build(qwm, name, [0, 1], sizes)
+    ctx.set_attend_kernel(4)
+    q = synth.queries(wl, 1, [0, 1], m=300)
+    got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
+    assert ctx.status() == 0
+    want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, q, [0, 1], 1 / np.sqrt(128))
+    err = np.abs(got - want).max()
+    assert err <= 1e-2 * vmax, (err, vmax)
