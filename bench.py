@@ -18,7 +18,9 @@ bounded sample of the same step on the host cores.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -36,6 +38,22 @@ from bit_kv_cache_qwm_gb300 import synth  # noqa: E402
 WORKLOAD = "bf16-h12-n32760"
 METRIC = "qwm_attend TFLOP/s & cache GB/s (% roofline); qwm_append Mtokens/s"
 L2_FLUSH_BYTES = 512 << 20
+
+
+def profiled_traffic(summary, source):
+    """DRAM bytes (read + write) per launch of the attention kernel from a
+    committed ncu summary, when the summary records the sha256 of the kernel
+    source it was captured on and that source is unchanged; else None."""
+    try:
+        with open(summary) as f:
+            text = f.read()
+        want = re.search(r"source sha256: ([0-9a-f]{64})", text).group(1)
+        nbytes = float(re.search(r"dram bytes per launch: ([0-9.eE+]+)", text).group(1))
+        with open(source, "rb") as f:
+            have = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, AttributeError, ValueError):
+        return None
+    return nbytes if have == want else None
 
 
 def attend_flops(H, M, N, d, r):
@@ -350,11 +368,15 @@ def run_gpu(args):
                        "append_gbs": H * wl.chunk * (4 * d + ctx.layout.bytes_per_token) / (float(np.mean(app)) * 1e-3) / 1e9,
                        "attend_kernel": kernel.get(ctx.resolved_attend_kernel, "?")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": profiled_traffic(os.path.join(ROOT, "profiles", f"attend_tc2_{wl.name}.md"),
+                                                 os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc", "attend_tc.cu"))
+                     if ctx.resolved_attend_kernel == 4 else None,
                      "kernel": "qwm_attend", "peak_source": peaks["source"] + " burst bf16"},
         "e2e": {"value": world * flops / (e2e_step * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step},
-        "gpu_launches": args.steps * 5,   # gram, eig, weights, append, attend
+        # gram, gram sum, A^2, eig, weights, append, attend (A^2 only when r > 0)
+        "gpu_launches": args.steps * (7 if r > 0 else 6),
         "clocks": clk.summary(),
         "wall_s": t_wall,
         "device_status": int(st),
