@@ -393,6 +393,91 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_small_m(args):
+    """Few query rows (--small-m M) over the workload's whole cache: the
+    attention is bound by reading the packed cache, so the metric is cache
+    GB/s against the measured HBM copy bandwidth.  Prints its own JSON line."""
+    import torch
+    from bit_kv_cache_qwm_gb300 import build as B
+    B.build()
+    from bit_kv_cache_qwm_gb300 import qwm
+    wl = synth.workload(args.workload)
+    H, d, r, C, M = wl.heads, wl.head_dim, wl.rank, wl.n_centroids, args.small_m
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev, torch.bfloat16)
+    kf = synth.kmeans_keys(wl)
+    rows = np.stack([synth.kmeans_init_rows(wl, h, kf.shape[1], C) for h in range(H)]).astype(np.int32)
+    tiles = wl.n_chunks * ((wl.chunk + 127) // 128)
+    ctx = qwm.Qwm(H, d, r, C, dtype=wl.dtype, max_tokens=tiles * 128, max_hist=wl.n_hist, device=dev)
+    ctx.set_centroids(qwm.qwm_kmeans(T(kf), torch.from_numpy(rows).to(dev), C, iters=25))
+    ctx.calibrate(T(synth.hist_queries(wl, 0)))
+    for ch in range(wl.n_chunks):
+        ctx.append(T(synth.keys(wl, ch)), T(synth.values(wl, ch)))
+    ctx.set_attend_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4}[args.kernel])
+    q = T(synth.queries(wl, 0, m=M))
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0, "device status bits after set-up"
+    N = wl.n_tokens
+    nbytes = H * N * ctx.layout.bytes_per_token + 2 * q.numel() * q.element_size()   # cache + Q + O
+    kern = ctx.attend_kernel_for(M)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        ctx.attend(q, out)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as clk:
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record(stream)
+            ctx.attend(q, out)
+            e1.record(stream)
+        torch.cuda.synchronize()
+    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+    st = ctx.status()
+    # end to end: Q from pinned host memory, O back to it, inside the timed region
+    h_q = q.cpu().pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    d_q = torch.empty_like(q)
+    e2e = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        d_q.copy_(h_q, non_blocking=True)
+        ctx.attend(d_q, out)
+        h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e.append(e0.elapsed_time(e1))
+    e2e_ms = float(np.mean(e2e))
+    peaks = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"qwm_attend cache GB/s, {M} query rows", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "heads": H, "head_dim": d, "cached_tokens": N, "query_rows": M,
+                   "n_centroids": C, "rank": r, "l2": "flushed between steps (512 MiB write)",
+                   "attend_kernel": kern},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "qwm_attend",
+                     "bytes_per_launch": nbytes, "peak_source": peaks["source"] + " HBM copy"},
+        "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": q.numel() * q.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size(), "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps * (3 if kern == 5 else 1),
+        "clocks": clk.summary(),
+        "device_status": int(st),
+        "attend_tflops": attend_flops(H, M, N, d, r) / (ms * 1e-3) / 1e12,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -405,8 +490,12 @@ def main():
                     help="profiling mode: set up the workload, then run only this call --steps times")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma", "tc", "tc2"],
                     help="attention kernel (auto picks the fastest that applies)")
+    ap.add_argument("--small-m", type=int, default=0,
+                    help="few-row attention: M query rows over the workload's whole cache (GB/s line)")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.small_m > 0 and args.impl != "reference":
+        run_small_m(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

@@ -78,7 +78,7 @@ extern "C" qwm_status qwm_sizes(const qwm_config* c, qwm_layout* out) {
   L.st_tiles = o;     o = align256(o + (size_t)L.max_tiles * 8);
   L.st_iters = o;     o = align256(o + H * 4);
   L.state_bytes = o;
-  L.workspace_bytes = align256(gram_workspace_bytes(*c));
+  L.workspace_bytes = align256(small_workspace_offset(*c) + small_workspace_bytes(*c));
   *out = L;
   return QWM_OK;
 }
@@ -248,11 +248,13 @@ extern "C" qwm_status qwm_attend(qwm_ctx* x, const void* d_q, int64_t M, float s
   if (x->n_tokens == 0) return QWM_ERR_INVALID_ARG;
   if (M > (int64_t)1 << 31) return QWM_ERR_INVALID_ARG;
   if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)x->cfg.head_dim);
-  int k = qwm_resolved_attend_kernel(x);
+  int k = qwm_attend_kernel_for(x, M);
+  if (k == 5 && !attend_small_supported(x, M)) return QWM_ERR_UNSUPPORTED;
   if (k == 2 && !attend_mma_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 3 && !attend_tc_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 4 && !attend_tc2_supported(x)) return QWM_ERR_UNSUPPORTED;
-  cudaError_t e = k == 4   ? launch_attend_tc2(x, d_q, M, scale, d_out, S(stream))
+  cudaError_t e = k == 5   ? launch_attend_small(x, d_q, M, scale, d_out, x->ws + small_workspace_offset(x->cfg), S(stream))
+                  : k == 4 ? launch_attend_tc2(x, d_q, M, scale, d_out, S(stream))
                   : k == 3 ? launch_attend_tc(x, d_q, M, scale, d_out, S(stream))
                   : k == 2 ? launch_attend_mma(x, d_q, M, scale, d_out, S(stream))
                            : launch_attend_simt(x, d_q, M, scale, d_out, S(stream));
@@ -293,9 +295,16 @@ extern "C" qwm_status qwm_get_status(qwm_ctx* x, void* stream) {
 }
 
 extern "C" qwm_status qwm_set_attend_kernel(qwm_ctx* x, int32_t k) {
-  if (!x || k < 0 || k > 4) return QWM_ERR_INVALID_ARG;
+  if (!x || k < 0 || k > 5) return QWM_ERR_INVALID_ARG;
   x->attend_kernel = k;
   return QWM_OK;
+}
+
+extern "C" int32_t qwm_attend_kernel_for(const qwm_ctx* x, int64_t M) {
+  if (!x) return -1;
+  if (x->attend_kernel != 0) return x->attend_kernel;
+  if (attend_small_supported(x, M)) return 5;
+  return qwm_resolved_attend_kernel(x);
 }
 
 extern "C" int32_t qwm_resolved_attend_kernel(const qwm_ctx* x) {

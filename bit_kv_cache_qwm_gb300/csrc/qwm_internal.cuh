@@ -75,6 +75,14 @@ bool attend_tc2_supported(const qwm_ctx* c);
 cudaError_t launch_attend_tc2(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
                               cudaStream_t st);
 size_t gram_workspace_bytes(const qwm_config& cfg);
+// few-row attention (M <= 64): its workspace follows the calibration's
+size_t small_workspace_bytes(const qwm_config& cfg);
+bool attend_small_supported(const qwm_ctx* c, int64_t M);
+cudaError_t launch_attend_small(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                                uint8_t* ws, cudaStream_t st);
+inline size_t small_workspace_offset(const qwm_config& cfg) {
+  return (gram_workspace_bytes(cfg) + 255) & ~size_t(255);
+}
 
 // ---- device helpers ----
 __device__ __forceinline__ float load_elem(const float* p, int64_t i) { return p[i]; }

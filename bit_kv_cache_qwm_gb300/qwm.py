@@ -53,8 +53,8 @@ class QwmError(RuntimeError):
 EXPORTS = ["qwm_status_string", "qwm_sizes", "qwm_create", "qwm_destroy", "qwm_set_centroids",
            "qwm_calibrate", "qwm_calibrate_static", "qwm_kmeans", "qwm_kmeans_workspace_bytes", "qwm_set_calibration", "qwm_get_calibration", "qwm_append",
            "qwm_attend", "qwm_rewind", "qwm_get_status", "qwm_peek_status_bits",
-           "qwm_set_attend_kernel", "qwm_resolved_attend_kernel", "qwm_num_tokens", "qwm_num_tiles", "qwm_num_segments",
-           "qwm_version"]
+           "qwm_set_attend_kernel", "qwm_resolved_attend_kernel", "qwm_attend_kernel_for", "qwm_num_tokens",
+           "qwm_num_tiles", "qwm_num_segments", "qwm_version"]
 
 _lib = None
 
@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     L.qwm_kmeans_workspace_bytes.restype = ctypes.c_size_t
     L.qwm_kmeans_workspace_bytes.argtypes = [I32, I32, I32, I64]
+    L.qwm_attend_kernel_for.restype = I32
+    L.qwm_attend_kernel_for.argtypes = [VP, I64]
     for name, rt in [("qwm_resolved_attend_kernel", I32), ("qwm_num_tokens", I64), ("qwm_num_tiles", I64), ("qwm_num_segments", I32),
                      ("qwm_version", I32)]:
         fn = getattr(L, name)
@@ -273,7 +275,12 @@ class Qwm:
 
     @property
     def resolved_attend_kernel(self) -> int:
+        """The attention kernel for more than 64 query rows."""
         return int(lib().qwm_resolved_attend_kernel(self._h))
+
+    def attend_kernel_for(self, m: int) -> int:
+        """The attention kernel qwm_attend runs for m query rows."""
+        return int(lib().qwm_attend_kernel_for(self._h, int(m)))
 
     @property
     def n_tokens(self) -> int:

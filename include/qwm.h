@@ -80,7 +80,8 @@ typedef struct {
 typedef struct {
   size_t cache_bytes;      /* H * max_tiles * tile_bytes                        */
   size_t state_bytes;      /* calibration, centroids, bases, tile table, status */
-  size_t workspace_bytes;  /* calibrate scratch                                 */
+  size_t workspace_bytes;  /* calibrate scratch, then the few-row attention's   */
+                           /* partial results (bf16, d = 128)                    */
   size_t tile_bytes;       /* bytes of one 128-slot tile of one head            */
   size_t bytes_per_token;  /* tile_bytes / 128                                  */
   int64_t max_tiles;       /* tiles per head                                    */
@@ -222,16 +223,23 @@ qwm_status qwm_kmeans(int32_t heads, int32_t head_dim, int32_t dtype, int32_t n_
                       const void* d_keys, int64_t n, const int32_t* d_init_rows, int32_t iters,
                       void* d_centroids, void* d_workspace, void* stream);
 
-/* Attention kernel choice: 0 = automatic (bf16 and d = 128: kernel 4 when
- * r <= 16, kernel 3 when r <= 32; otherwise kernel 2 where it applies, else
- * kernel 1), 1 = float32 CUDA-core kernel, 2 = bf16 mma.sync kernel, 3 = bf16
- * tcgen05 kernel with 128 query rows per CTA, 4 = bf16 tcgen05 kernel with 256
- * query rows per CTA (r <= 16).  An explicit choice the configuration does not
- * support makes qwm_attend return QWM_ERR_UNSUPPORTED. */
+/* Attention kernel choice: 0 = automatic (bf16 and d = 128: kernel 5 when
+ * M <= 64 and r <= 32, else kernel 4 when r <= 16, kernel 3 when r <= 32;
+ * otherwise kernel 2 where it applies, else kernel 1), 1 = float32 CUDA-core
+ * kernel, 2 = bf16 mma.sync kernel, 3 = bf16 tcgen05 kernel with 128 query
+ * rows per CTA, 4 = bf16 tcgen05 kernel with 256 query rows per CTA
+ * (r <= 16), 5 = bf16 kernel for at most 64 query rows (split over the cache
+ * tiles, partial results in the context workspace, merged by a second
+ * kernel).  An explicit choice the configuration (or M) does not support makes
+ * qwm_attend return QWM_ERR_UNSUPPORTED. */
 qwm_status qwm_set_attend_kernel(qwm_ctx* ctx, int32_t kernel);
 
-/* The attention kernel qwm_attend will run (1 to 4; automatic resolved). */
+/* The attention kernel qwm_attend runs for more than 64 query rows (1 to 4;
+ * automatic resolved). */
 int32_t qwm_resolved_attend_kernel(const qwm_ctx* ctx);
+
+/* The attention kernel qwm_attend runs for M query rows (1 to 5). */
+int32_t qwm_attend_kernel_for(const qwm_ctx* ctx, int64_t M);
 
 int64_t qwm_num_tokens(const qwm_ctx* ctx);    /* valid tokens cached        */
 int64_t qwm_num_tiles(const qwm_ctx* ctx);     /* tiles in use per head      */
