@@ -172,6 +172,33 @@ def qsac_assign(k32, C32, w32) -> np.ndarray:
     return out
 
 
+def nearest_scores_f32(k32, C32) -> np.ndarray:
+    """Squared distance of one key to every centroid, the decision of the
+    nearest-centroid assignment that [B] Step 1 describes for QVG (each key is
+    assigned to the centre it is closest to), in float32 with a fixed order:
+    rho = f32(k - C_j); D_g = float32 sum over the 32 channels of group g, in
+    channel order, of f32(rho * rho); S_j = the same tree sum over groups as
+    the QSAC score.  k32 [d], C32 [C, d] -> S [C] float32."""
+    k = np.asarray(k32, dtype=f32)
+    C = np.asarray(C32, dtype=f32)
+    rho = (k[None, :] - C).astype(f32)
+    nC, d = rho.shape
+    sq = (rho * rho).astype(f32).reshape(nC, d // GROUP, GROUP)
+    acc = sq[..., 0].copy()
+    for c in range(1, GROUP):
+        acc = (acc + sq[..., c]).astype(f32)
+    return _score_tree(acc)
+
+
+def nearest_assign(k32, C32) -> np.ndarray:
+    """Nearest centroid for every key row of k32 [n, d]; lowest index on a tie."""
+    k = np.asarray(k32, dtype=f32)
+    out = np.empty(k.shape[0], dtype=np.int64)
+    for i in range(k.shape[0]):
+        out[i] = int(np.argmin(nearest_scores_f32(k[i], C32)))
+    return out
+
+
 # --------------------------------------------------------------------------
 # per-group asymmetric INT2 quantiser and 2-bit packing  [A], [B Step 1]
 # --------------------------------------------------------------------------
@@ -266,15 +293,21 @@ class Segment:
     saturated: int = 0
 
 
-def append_head(k32, v32, C32, w32, U, version: int = 0) -> Segment:
+def append_head(k32, v32, C32, w32, U, version: int = 0, assign: str = "qsac") -> Segment:
     """Encode one chunk of one head.  k32, v32 [n, d] float32; C32 [C, d]
     float32 (centroids already rounded to the cache dtype); w32 [G] float32;
-    U [r, d] float64 (rows = basis vectors)."""
+    U [r, d] float64 (rows = basis vectors).  assign: "qsac" (QuantWM) or
+    "nearest" (the nearest-centroid baseline)."""
     k = np.asarray(k32, dtype=f32)
     v = np.asarray(v32, dtype=f32)
     C = np.asarray(C32, dtype=f32)
     U = np.asarray(U, dtype=np.float64).reshape(-1, k.shape[1])
-    idx = qsac_assign(k, C, w32)
+    if assign == "nearest":
+        idx = nearest_assign(k, C)
+    elif assign == "qsac":
+        idx = qsac_assign(k, C, w32)
+    else:
+        raise ValueError(f"unknown assignment {assign!r}")
     rho = (k - C[idx]).astype(f32)                   # residual of the chosen centroid
     kz, ks, kc, ksat = quantize_rows(rho)
     khat = C[idx].astype(np.float64) + dequantize_rows(kz, ks, kc)
@@ -459,8 +492,9 @@ class OracleCache:
     its coefficients in that version's basis.
     """
 
-    def __init__(self, heads: int, d: int, r: int, centroids32):
+    def __init__(self, heads: int, d: int, r: int, centroids32, assign: str = "qsac"):
         self.H, self.d, self.r = heads, d, r
+        self.assign = assign
         self.C = np.asarray(centroids32, dtype=f32)        # [H, C, d]
         self.version = -1
         self.w = None
@@ -478,9 +512,73 @@ class OracleCache:
         hs = range(self.H) if heads is None else heads
         for i, h in enumerate(hs):
             self.segments[h].append(append_head(k32[i], v32[i], self.C[h], self.w[h],
-                                                self.bases[h][self.version], self.version))
+                                                self.bases[h][self.version], self.version, self.assign))
 
     def attend(self, q, sigma: float, heads=None) -> np.ndarray:
         hs = range(self.H) if heads is None else heads
         return np.stack([attend_head(q[i], self.segments[h], self.bases[h], sigma)
                          for i, h in enumerate(hs)])
+
+
+# --------------------------------------------------------------------------
+# attention-shift diagnostics  [A] Abstract; [B] "The key to a smaller
+# error ...", Figure 2, Table 1
+# --------------------------------------------------------------------------
+
+def compensated_logits(q, segments, bases, e_exact: bool = False) -> np.ndarray:
+    """l [M, N] = q . k_hat_n + (q U_t^T) . e_n over all segments (float64)."""
+    q = np.asarray(q, dtype=np.float64)
+    out = []
+    for seg in segments:
+        l = q @ seg.khat.T
+        U = np.asarray(bases[seg.version], dtype=np.float64)
+        if U.shape[0] > 0:
+            e = seg.e64 if e_exact else seg.e16.astype(np.float64)
+            l = l + (q @ U.T) @ e.T
+        out.append(l)
+    return np.concatenate(out, axis=1)
+
+
+def top1_change(logits_exact, logits_quant) -> float:
+    """Fraction of query rows whose highest-scoring cached token differs
+    between the exact and the quantised logits (the Table 1 measure)."""
+    a = np.argmax(np.asarray(logits_exact), axis=1)
+    b = np.argmax(np.asarray(logits_quant), axis=1)
+    return float(np.mean(a != b))
+
+
+def softmax_rows(logits, sigma: float) -> np.ndarray:
+    L = sigma * np.asarray(logits, dtype=np.float64)
+    L = L - L.max(axis=1, keepdims=True)
+    P = np.exp(L)
+    return P / P.sum(axis=1, keepdims=True)
+
+
+def key_value_study(q, k, v, segments, bases, sigma: float) -> dict:
+    """Key-only vs value-only quantisation of one head ([B], "The key to a
+    smaller error ..."): relative reconstruction errors of K and V, and the
+    relative output error when only K (PSAC included) or only V is taken from
+    the cache, the other one exact.  q [M, d], k, v [N, d] (float, in cache
+    order)."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    khat = np.concatenate([s.khat for s in segments])
+    vhat = np.concatenate([s.vhat for s in segments])
+    o = softmax_rows(q @ k.T, sigma) @ v
+    o_k = softmax_rows(compensated_logits(q, segments, bases), sigma) @ v
+    o_v = softmax_rows(q @ k.T, sigma) @ vhat
+    nrm = np.linalg.norm
+    return {"key_rel_error": float(nrm(k - khat) / nrm(k)),
+            "value_rel_error": float(nrm(v - vhat) / nrm(v)),
+            "output_rel_error_key_only": float(nrm(o_k - o) / nrm(o)),
+            "output_rel_error_value_only": float(nrm(o_v - o) / nrm(o))}
+
+
+def logit_error(q, k, segments, bases) -> float:
+    """Root mean square of q . k - l_quant over all (query, token) pairs,
+    relative to the root mean square of q . k."""
+    q = np.asarray(q, dtype=np.float64)
+    exact = q @ np.asarray(k, dtype=np.float64).T
+    d = exact - compensated_logits(q, segments, bases)
+    return float(np.sqrt(np.mean(d * d) / np.mean(exact * exact)))
