@@ -17,7 +17,9 @@
 // score of a centroid is formed exactly as the decision definition states:
 // f32 residual, exact max/min (their evaluation order does not matter), R*R,
 // w*R^2, fixed tree sum, strict < in ascending index order so the lowest
-// index wins a tie.
+// index wins a tie.  NEAREST replaces the score by the squared distance (the
+// nearest-centroid baseline): per group a float32 sum of f32(rho*rho) in
+// channel order, the same tree over groups.
 #include "qwm_internal.cuh"
 
 namespace qwm {
@@ -109,7 +111,7 @@ __device__ __forceinline__ uint32_t quantize32(const float* x, uint2* packed, fl
   return (uint32_t)__half_as_ushort(zh) | ((uint32_t)__half_as_ushort(sh) << 16);
 }
 
-template <int D, typename T>
+template <int D, typename T, bool NEAREST>
 __global__ void __launch_bounds__(kTile * (D / kGroup))
 append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
               const T* __restrict__ cent, int nC, const float* __restrict__ w,
@@ -153,6 +155,30 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
     for (int i = threadIdx.x; i < cn * D; i += NT)
       cs[(i / D) * RS + ((i % D) / kGroup) * GS + (i % kGroup)] = -load_elem(ch + (int64_t)c0 * D, i);
     __syncthreads();
+    if constexpr (NEAREST) {
+#pragma unroll 1
+      for (int j = 0; j < cn; ++j) {
+        const float* cr = cs + j * RS + gi * GS;
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float dlt = __fadd_rn(kx[i], cr[i]);
+          acc = __fadd_rn(acc, __fmul_rn(dlt, dlt));
+        }
+        float S;
+        if (G == 4) {
+          const float u = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, TPW));
+          S = __fadd_rn(u, __shfl_xor_sync(kFull, u, 2 * TPW));
+        } else {
+          S = __fadd_rn(acc, __shfl_xor_sync(kFull, acc, TPW));
+        }
+        if (S < best) {
+          best = S;
+          bj = c0 + j;
+        }
+      }
+      continue;
+    }
     // two centroids per step, each with even/odd partial max/min: eight
     // independent dependency chains per thread
 #pragma unroll 1
@@ -264,7 +290,7 @@ cudaError_t launch_t(const qwm_ctx* c, const void* k, const void* v, int64_t n, 
   const int r = c->cfg.rank, H = c->cfg.heads, nC = c->cfg.n_centroids;
   constexpr int CH = 16384 / D;
   const size_t smem = (size_t)CH * (D / kGroup) * (kGroup + 4) * 4 + (size_t)r * D * 4;
-  auto kern = append_kernel<D, T>;
+  auto kern = c->assign == 1 ? append_kernel<D, T, true> : append_kernel<D, T, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((n + kTile - 1) / kTile), (unsigned)H);

@@ -122,6 +122,7 @@ extern "C" qwm_status qwm_create(const qwm_config* c, void* d_cache, void* d_sta
   x->slot = -1;
   x->centroids_set = false;
   x->attend_kernel = 0;
+  x->assign = 0;
   if (cudaMemset(d_state, 0, L.state_bytes) != cudaSuccess ||
       cudaDeviceSynchronize() != cudaSuccess) {
     delete x;
@@ -292,6 +293,18 @@ extern "C" qwm_status qwm_get_status(qwm_ctx* x, void* stream) {
   if (bits & QWM_DEV_NOT_CONVERGED) return QWM_ERR_NOT_CONVERGED;
   if (bits) return QWM_ERR_DEVICE;
   return QWM_OK;
+}
+
+extern "C" qwm_status qwm_set_assignment(qwm_ctx* x, int32_t mode) {
+  if (!x || mode < 0 || mode > 1) return QWM_ERR_INVALID_ARG;
+  x->assign = mode;
+  return QWM_OK;
+}
+
+extern "C" qwm_status qwm_dequantize(qwm_ctx* x, float* d_khat, float* d_vhat, float* d_e, void* stream) {
+  if (!x || !d_khat || !d_vhat || (x->cfg.rank > 0 && !d_e)) return QWM_ERR_INVALID_ARG;
+  if (!x->centroids_set) return QWM_ERR_NOT_CALIBRATED;
+  return cuda_status(launch_dequantize(x, d_khat, d_vhat, d_e, S(stream)));
 }
 
 extern "C" qwm_status qwm_set_attend_kernel(qwm_ctx* x, int32_t k) {

@@ -52,6 +52,7 @@ struct qwm_ctx {
   int32_t slot;          // basis slot of the current version
   bool centroids_set;
   int32_t attend_kernel;
+  int32_t assign;        // 0 QSAC, 1 nearest centroid
   std::vector<qwm::SegmentRec> segs;
 };
 
@@ -63,6 +64,7 @@ cudaError_t launch_append(const qwm_ctx* c, const void* k, const void* v, int64_
 cudaError_t launch_gram(const qwm_ctx* c, const void* q, int64_t n_h, cudaStream_t st);
 cudaError_t launch_eig(const qwm_ctx* c, int64_t n_h, int32_t version, cudaStream_t st);
 cudaError_t launch_group_weights(const qwm_ctx* c, cudaStream_t st);
+cudaError_t launch_dequantize(const qwm_ctx* c, float* khat, float* vhat, float* e, cudaStream_t st);
 cudaError_t launch_attend_simt(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
                                cudaStream_t st);
 cudaError_t launch_attend_mma(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,

@@ -53,7 +53,8 @@ class QwmError(RuntimeError):
 EXPORTS = ["qwm_status_string", "qwm_sizes", "qwm_create", "qwm_destroy", "qwm_set_centroids",
            "qwm_calibrate", "qwm_calibrate_static", "qwm_kmeans", "qwm_kmeans_workspace_bytes", "qwm_set_calibration", "qwm_get_calibration", "qwm_append",
            "qwm_attend", "qwm_rewind", "qwm_get_status", "qwm_peek_status_bits",
-           "qwm_set_attend_kernel", "qwm_resolved_attend_kernel", "qwm_attend_kernel_for", "qwm_num_tokens",
+           "qwm_set_attend_kernel", "qwm_resolved_attend_kernel", "qwm_attend_kernel_for", "qwm_set_assignment",
+           "qwm_dequantize", "qwm_num_tokens",
            "qwm_num_tiles", "qwm_num_segments", "qwm_version"]
 
 _lib = None
@@ -84,6 +85,8 @@ def lib() -> ctypes.CDLL:
         "qwm_get_status": [VP, VP],
         "qwm_peek_status_bits": [VP, P(ctypes.c_uint32), VP],
         "qwm_set_attend_kernel": [VP, I32],
+        "qwm_set_assignment": [VP, I32],
+        "qwm_dequantize": [VP, VP, VP, VP, VP],
         "qwm_calibrate_static": [I32, I32, I32, I32, I32, I32, VP, I64, VP, VP, VP, VP, VP, VP],
         "qwm_kmeans": [I32, I32, I32, I32, VP, I64, VP, I32, VP, VP, VP],
     }
@@ -269,6 +272,24 @@ class Qwm:
         b = ctypes.c_uint32(0)
         _check(lib().qwm_peek_status_bits(self._h, ctypes.byref(b), _stream()), "qwm_peek_status_bits")
         return int(b.value)
+
+    def set_assignment(self, mode: str):
+        """Centroid assignment of later appends: "qsac" or "nearest"."""
+        _check(lib().qwm_set_assignment(self._h, {"qsac": 0, "nearest": 1}[mode]), "qwm_set_assignment")
+
+    def dequantize(self):
+        """(k_hat, v_hat, e) float32 [H, n_tiles*128, d / d / r] and the valid
+        slot mask [n_tiles*128] (cache order)."""
+        H, d, r = self.cfg.heads, self.cfg.head_dim, self.cfg.rank
+        n = self.n_tiles * 128
+        kh = torch.empty((H, n, d), dtype=torch.float32, device=self.device)
+        vh = torch.empty((H, n, d), dtype=torch.float32, device=self.device)
+        e = torch.empty((H, n, max(r, 1)), dtype=torch.float32, device=self.device)
+        _check(lib().qwm_dequantize(self._h, ctypes.c_void_p(kh.data_ptr()), ctypes.c_void_p(vh.data_ptr()),
+                                    ctypes.c_void_p(e.data_ptr()), _stream()), "qwm_dequantize")
+        counts = self.tile_table()[: self.n_tiles, 1].to(torch.int64)
+        valid = (torch.arange(128, device=counts.device)[None, :] < counts[:, None]).reshape(-1)
+        return kh, vh, e[..., :r], valid
 
     def set_attend_kernel(self, k: int):
         _check(lib().qwm_set_attend_kernel(self._h, int(k)), "qwm_set_attend_kernel")

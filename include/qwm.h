@@ -223,6 +223,19 @@ qwm_status qwm_kmeans(int32_t heads, int32_t head_dim, int32_t dtype, int32_t n_
                       const void* d_keys, int64_t n, const int32_t* d_init_rows, int32_t iters,
                       void* d_centroids, void* d_workspace, void* stream);
 
+/* Centroid assignment of later appends: 0 = QSAC (default; the
+ * sensitivity-weighted residual-range score), 1 = nearest centroid (squared
+ * distance), the baseline the roboind article's "Step 1" describes for QVG and
+ * that QSAC replaces.  For comparisons (the attention-shift diagnostics). */
+qwm_status qwm_set_assignment(qwm_ctx* ctx, int32_t mode);
+
+/* The cache in float32 for analysis: k_hat [H][n_tiles*128][d] =
+ * C[j] + zero + code*scale, v_hat [H][n_tiles*128][d] = zero + code*scale,
+ * e [H][n_tiles*128][r] (the stored fp16 coefficients; may be NULL when
+ * r = 0), slot s of tile t at row t*128 + s; pad slots are zero.  Caller-owned
+ * device buffers.  Asynchronous. */
+qwm_status qwm_dequantize(qwm_ctx* ctx, float* d_khat, float* d_vhat, float* d_e, void* stream);
+
 /* Attention kernel choice: 0 = automatic (bf16 and d = 128: kernel 5 when
  * M <= 64 and r <= 32, else kernel 4 when r <= 16, kernel 3 when r <= 32;
  * otherwise kernel 2 where it applies, else kernel 1), 1 = float32 CUDA-core
