@@ -180,6 +180,15 @@ __device__ __forceinline__ __half2 codes_h2(uint32_t n) {
   const uint32_t w = 0x64006400u | (n & 3u) | (((n >> 2) & 3u) << 16);
   return __hsub2(*reinterpret_cast<const __half2*>(&w), __float2half2_rn(1024.f));
 }
+// Two 2-bit codes at bits p and p+2 of a 16-bit word n as exact floats,
+// without shifts: the code's bits are the low mantissa bits of a float whose
+// exponent makes bit p weigh 1 (2^(23-p) + c), minus 2^(23-p).
+template <int P>
+__device__ __forceinline__ float2 codes_at(uint32_t n) {
+  constexpr uint32_t e0 = (uint32_t)(127 + 23 - P) << 23, e1 = (uint32_t)(127 + 21 - P) << 23;
+  const float2 m = make_float2(__uint_as_float((n & (3u << P)) | e0), __uint_as_float((n & (12u << P)) | e1));
+  return __fadd2_rn(m, make_float2(-__uint_as_float(e0), -__uint_as_float(e1)));
+}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -223,6 +232,7 @@ struct TcArgs {
   int64_t n_tiles;
   const int2* tiles;
   const __nv_bfloat16* cent;
+  const float* cent32;   // float32 copy of the centroids
   int nC;
   const float* basis;
   int H;
@@ -971,11 +981,13 @@ __global__ void __launch_bounds__(kThreads2, 1) attend_tc2_kernel(const TcArgs a
         const float kz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
         const float ks = __half2float(__ushort_as_half((unsigned short)(qp >> 16)));
         const float2 kz2 = make_float2(kz, kz), ks2 = make_float2(ks, ks);
-        uint4 craw[4];
+        const float* c32 = a.cent32 + ((int64_t)h * a.nC + idx) * kD;
+        float4 craw[8];
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           const int chunk = grp * 4 + ((c8 + grp) & 3);
-          craw[c8] = __ldg(reinterpret_cast<const uint4*>(ch + (int64_t)idx * kD + 8 * chunk));
+          craw[2 * c8] = __ldg(reinterpret_cast<const float4*>(c32 + 8 * chunk));
+          craw[2 * c8 + 1] = __ldg(reinterpret_cast<const float4*>(c32 + 8 * chunk + 4));
         }
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
@@ -983,15 +995,16 @@ __global__ void __launch_bounds__(kThreads2, 1) attend_tc2_kernel(const TcArgs a
           // (2 keys x 4 groups) then hit 8 different bank groups
           const int cl = (c8 + grp) & 3;
           const int chunk = grp * 4 + cl;
-          const uint32_t cw[4] = {craw[c8].x, craw[c8].y, craw[c8].z, craw[c8].w};
+          const float2 cc4[4] = {make_float2(craw[2 * c8].x, craw[2 * c8].y), make_float2(craw[2 * c8].z, craw[2 * c8].w),
+                                 make_float2(craw[2 * c8 + 1].x, craw[2 * c8 + 1].y),
+                                 make_float2(craw[2 * c8 + 1].z, craw[2 * c8 + 1].w)};
           const uint32_t bits = ((cl >> 1) ? kc.y : kc.x) >> (16 * (cl & 1)) & 0xffffu;
+          const float2 cds[4] = {codes_at<0>(bits), codes_at<4>(bits), codes_at<8>(bits), codes_at<12>(bits)};
           uint32_t ph[4], pl[4];
 #pragma unroll
           for (int e2 = 0; e2 < 4; ++e2) {
-            const float2 cd = codes_f2(bits >> (4 * e2));
-            const float2 rq = __ffma2_rn(cd, ks2, kz2);                      // zero + code*scale
-            const float2 cc = make_float2(__uint_as_float(cw[e2] << 16), __uint_as_float(cw[e2] & 0xffff0000u));
-            const float2 kv = __fadd2_rn(cc, rq);                            // + centroid
+            const float2 rq = __ffma2_rn(cds[e2], ks2, kz2);                 // zero + code*scale
+            const float2 kv = __fadd2_rn(cc4[e2], rq);                       // + centroid
             const __nv_bfloat162 hb = __floats2bfloat162_rn(kv.x, kv.y);
             const float2 hf = __bfloat1622float2(hb);
             const float2 lo = __fadd2_rn(kv, make_float2(-hf.x, -hf.y));
@@ -1301,6 +1314,7 @@ TcArgs tc_args(const qwm_ctx* c, const void* q, int64_t M, float scale, void* ou
   a.n_tiles = c->n_tiles;
   a.tiles = c->tiles;
   a.cent = (const __nv_bfloat16*)c->centroids;
+  a.cent32 = c->cent32;
   a.nC = c->cfg.n_centroids;
   a.basis = c->basis;
   a.H = c->cfg.heads;

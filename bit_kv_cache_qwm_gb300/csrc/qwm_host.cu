@@ -77,6 +77,12 @@ extern "C" qwm_status qwm_sizes(const qwm_config* c, qwm_layout* out) {
   L.st_basis = o;     o = align256(o + (size_t)c->max_versions * H * (r > 0 ? r : 1) * d * 4);
   L.st_tiles = o;     o = align256(o + (size_t)L.max_tiles * 8);
   L.st_iters = o;     o = align256(o + H * 4);
+  if (c->dtype == QWM_BF16) {
+    L.st_centroids_f32 = o;
+    o = align256(o + (size_t)H * c->n_centroids * d * 4);
+  } else {
+    L.st_centroids_f32 = L.st_centroids;
+  }
   L.state_bytes = o;
   L.workspace_bytes = align256(small_workspace_offset(*c) + small_workspace_bytes(*c));
   *out = L;
@@ -113,6 +119,7 @@ extern "C" qwm_status qwm_create(const qwm_config* c, void* d_cache, void* d_sta
   x->lambda = (float*)(x->state + L.st_lambda);
   x->energy = (float*)(x->state + L.st_energy);
   x->centroids = (void*)(x->state + L.st_centroids);
+  x->cent32 = reinterpret_cast<float*>(x->state + L.st_centroids_f32);
   x->basis = (float*)(x->state + L.st_basis);
   x->tiles = (int2*)(x->state + L.st_tiles);
   x->iters = (int32_t*)(x->state + L.st_iters);
@@ -137,10 +144,22 @@ extern "C" qwm_status qwm_destroy(qwm_ctx* ctx) {
   return QWM_OK;
 }
 
+// float32 copy of the bf16 centroids (exact), read by the attention kernels
+static __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, float* __restrict__ out, int64_t n) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = __bfloat162float(in[i]);
+}
+
 extern "C" qwm_status qwm_set_centroids(qwm_ctx* x, const void* d_centroids, void* stream) {
   if (!x || !d_centroids) return QWM_ERR_INVALID_ARG;
   size_t bytes = (size_t)x->cfg.heads * x->cfg.n_centroids * x->cfg.head_dim * x->esz;
   cudaError_t e = cudaMemcpyAsync(x->centroids, d_centroids, bytes, cudaMemcpyDeviceToDevice, S(stream));
+  if (e == cudaSuccess && x->cfg.dtype == QWM_BF16) {
+    const int64_t n = (int64_t)x->cfg.heads * x->cfg.n_centroids * x->cfg.head_dim;
+    bf16_to_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, S(stream)>>>(
+        (const __nv_bfloat16*)x->centroids, x->cent32, n);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return QWM_ERR_CUDA;
   x->centroids_set = true;
   return QWM_OK;

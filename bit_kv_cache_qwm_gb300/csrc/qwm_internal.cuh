@@ -42,6 +42,7 @@ struct qwm_ctx {
   float* lambda;
   float* energy;
   void* centroids;
+  float* cent32;    // float32 copy of the centroids (bf16 configs)
   float* basis;     // [max_versions][H][r][d]
   int2* tiles;      // [max_tiles] (version, valid)
   int32_t* iters;   // [H] eigen-solver iterations of the last calibrate

@@ -41,7 +41,7 @@ class qwm_layout(ctypes.Structure):
                [(n, ctypes.c_size_t) for n in ("off_idx", "off_kcode", "off_kqp", "off_e", "off_vcode",
                                                 "off_vqp", "st_status", "st_s", "st_w", "st_lambda",
                                                 "st_energy", "st_centroids", "st_basis", "st_tiles",
-                                                "st_iters")]
+                                                "st_iters", "st_centroids_f32")]
 
 
 class QwmError(RuntimeError):

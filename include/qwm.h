@@ -89,6 +89,7 @@ typedef struct {
   size_t off_idx, off_kcode, off_kqp, off_e, off_vcode, off_vqp;
   /* offsets of the arrays inside the state buffer */
   size_t st_status, st_s, st_w, st_lambda, st_energy, st_centroids, st_basis, st_tiles, st_iters;
+  size_t st_centroids_f32;  /* float32 copy of bf16 centroids (= st_centroids for f32) */
 } qwm_layout;
 
 typedef struct qwm_ctx qwm_ctx;
