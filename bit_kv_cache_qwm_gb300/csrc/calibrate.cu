@@ -31,7 +31,8 @@ namespace {
 constexpr int kRowsPerSplit = 128;
 constexpr int kMaxSplits = 32;
 constexpr int kEigThreads = 256;
-constexpr int kCheckEvery = 2;       // A^2 iterations between Rayleigh-Ritz checks
+constexpr int kFirstCheck = 4;       // A^2 iterations before the first Rayleigh-Ritz check
+constexpr int kCheckEvery = 2;       // ... and between later checks
 constexpr float kResidualTol = 2e-6f;
 constexpr float kShift = 9.5367431640625e-07f;   // 2^-20 of the mean eigenvalue
 
@@ -719,9 +720,9 @@ __host__ __device__ inline EigLayout eig_layout(int d, int m) {
 // One CTA per head: the top-r eigenvectors of A = G * scale + shift.
 //   m < d: block subspace iteration on A^2 (from the square kernel, held in
 //     shared memory) from unit vectors at the m largest diagonal entries,
-//     orthonormalised by MGS2 every step; every kCheckEvery steps a
-//     Rayleigh-Ritz pass on A (Jacobi on X^T A X) and the residual test of
-//     the leading r Ritz pairs.
+//     orthonormalised by MGS2 every step; after kFirstCheck steps and then
+//     every kCheckEvery steps a Rayleigh-Ritz pass on A (Jacobi on X^T A X)
+//     and the residual test of the leading r Ritz pairs.
 //   m = d: Jacobi on the whole matrix.
 // Then the final Ritz vectors are re-orthonormalised and put through one more
 // Rayleigh-Ritz pass, which restores orthogonality to float32 precision.
@@ -799,7 +800,7 @@ eig_kernel(const float* __restrict__ part, int splits, const float* __restrict__
     }
     __syncthreads();
     while (true) {
-      for (int t = 0; t < kCheckEvery && iters < max_iter; ++t, ++iters) {
+      for (int t = 0, n = iters == 0 ? kFirstCheck : kCheckEvery; t < n && iters < max_iter; ++t, ++iters) {
         mm_bx<D, false>(A2s, D + 1, 1.f, X, ldx, W, ldx, m);
         orthonormalise<D>(W, X, ldx, m, colbuf, tmp);
       }
