@@ -422,7 +422,7 @@ __device__ __forceinline__ float rsqrt_nr(float x) {
 // ||v - f u||^2 = ||v||^2 - f^2 (u a unit vector); where that difference
 // cancels (below 1e-4 ||v||^2) the norm is summed again from the vector.
 template <int D, int C>
-__device__ void mgs2(const float* Xin, float* Xout, int ldx, int m, float* colbuf /* [2][D] */) {
+__device__ void mgs2(const float* Xin, float* Xout, int ldx, int m, float* colbuf /* [2][D] */, int passes) {
   constexpr int J = D / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float v[C][J];
@@ -434,10 +434,10 @@ __device__ void mgs2(const float* Xin, float* Xout, int ldx, int m, float* colbu
   }
   if (warp == 0) normalise_publish<J>(v[0], colbuf, lane);
   int step = 0;
-  for (int pass = 0; pass < 2; ++pass) {
+  for (int pass = 0; pass < passes; ++pass) {
     for (int j = 0; j < m; ++j, ++step) {
       int nx = j + 1;
-      if (nx == m) nx = pass == 0 ? 0 : -1;
+      if (nx == m) nx = pass + 1 < passes ? 0 : -1;
       const int sel = nx >= 0 ? nx >> 3 : 0;
       const bool owner = nx >= 0 && warp == (nx & 7);
       __syncthreads();
@@ -543,10 +543,14 @@ __device__ void mgs2_block(float* X, int ldx, int d, int m, float* tmp) {
   }
 }
 
+// passes = 2 (MGS twice: orthogonal to float32 precision) before a
+// Rayleigh-Ritz pass; 1 between checks, where the basis only has to stay well
+// conditioned, and on Ritz vectors that are orthonormal up to rounding.
 template <int D>
-__device__ void orthonormalise(const float* Xin, float* Xout, int ldx, int m, float* colbuf, float* tmp) {
-  if (m <= 32) mgs2<D, 4>(Xin, Xout, ldx, m, colbuf);
-  else if (m <= 64) mgs2<D, 8>(Xin, Xout, ldx, m, colbuf);
+__device__ void orthonormalise(const float* Xin, float* Xout, int ldx, int m, float* colbuf, float* tmp,
+                               int passes) {
+  if (m <= 32) mgs2<D, 4>(Xin, Xout, ldx, m, colbuf, passes);
+  else if (m <= 64) mgs2<D, 8>(Xin, Xout, ldx, m, colbuf, passes);
   else mgs2_block(Xout, ldx, D, m, tmp);   // whole-matrix path: Xin == Xout
 }
 
@@ -720,9 +724,10 @@ __host__ __device__ inline EigLayout eig_layout(int d, int m) {
 // One CTA per head: the top-r eigenvectors of A = G * scale + shift.
 //   m < d: block subspace iteration on A^2 (from the square kernel, held in
 //     shared memory) from unit vectors at the m largest diagonal entries,
-//     orthonormalised by MGS2 every step; after kFirstCheck steps and then
-//     every kCheckEvery steps a Rayleigh-Ritz pass on A (Jacobi on X^T A X)
-//     and the residual test of the leading r Ritz pairs.
+//     orthonormalised by MGS every step (twice before a check); after
+//     kFirstCheck steps and then every kCheckEvery steps a Rayleigh-Ritz pass
+//     on A (Jacobi on X^T A X) and the residual test of the leading r Ritz
+//     pairs.
 //   m = d: Jacobi on the whole matrix.
 // Then the final Ritz vectors are re-orthonormalised and put through one more
 // Rayleigh-Ritz pass, which restores orthogonality to float32 precision.
@@ -802,7 +807,8 @@ eig_kernel(const float* __restrict__ part, int splits, const float* __restrict__
     while (true) {
       for (int t = 0, n = iters == 0 ? kFirstCheck : kCheckEvery; t < n && iters < max_iter; ++t, ++iters) {
         mm_bx<D, false>(A2s, D + 1, 1.f, X, ldx, W, ldx, m);
-        orthonormalise<D>(W, X, ldx, m, colbuf, tmp);
+        const bool last = t + 1 == n || iters + 1 == max_iter;   // a check follows
+        orthonormalise<D>(W, X, ldx, m, colbuf, tmp, last ? 2 : 1);
       }
       // Rayleigh-Ritz on A and the residuals of the leading r Ritz pairs
       times_a(X, W);
@@ -837,7 +843,7 @@ eig_kernel(const float* __restrict__ part, int splits, const float* __restrict__
     }
   }
   // re-orthonormalise and one more Rayleigh-Ritz pass
-  orthonormalise<D>(X, X, ldx, m, colbuf, tmp);
+  orthonormalise<D>(X, X, ldx, m, colbuf, tmp, 1);
   times_a(X, W);
   project(X, ldx, W, ldx, H0, H1, ldh, D, m);
   set_identity(V, ldh, m);
