@@ -177,8 +177,7 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
           bj = c0 + j;
         }
       }
-      continue;
-    }
+    } else {
     // two centroids per step, each with even/odd partial max/min: eight
     // independent dependency chains per thread
 #pragma unroll 1
@@ -228,6 +227,7 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
         best = Sb;
         bj = c0 + j + 1;
       }
+    }
     }
   }
 

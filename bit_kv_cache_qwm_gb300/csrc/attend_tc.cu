@@ -900,7 +900,6 @@ __global__ void __launch_bounds__(kThreads2, 1) attend_tc2_kernel(const TcArgs a
   } else if (warp < kMmaWarp2) {
     // ------------------------------------------------------------ producers
     const int p = tid - kSoft2Warps * 32;      // 0..223
-    const __nv_bfloat16* ch = a.cent + (int64_t)h * a.nC * kD;
     int cur_slot = -1;
     bool ok = true;
     const uint32_t TB = (uint32_t)a.off.bytes;
@@ -1088,87 +1087,78 @@ __global__ void __launch_bounds__(kThreads2, 1) attend_tc2_kernel(const TcArgs a
     ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
     fence_after();
     // streams: S_a, S_b, PV_a, PV_b.  S_g(n) needs k_hat(n) and PV_g(n-1)
-    // issued; PV_g(n) needs S_g(n) issued, P_g(n) and v_hat(n).
-    int64_t nS[2] = {0, 0}, nP[2] = {0, 0};
-    long long last = clock64();
-    while (ok && (nP[0] < nt || nP[1] < nt)) {
-      bool did = false;
+    // issued; PV_g(n) needs S_g(n) issued, P_g(n) and v_hat(n).  The leader
+    // alone polls and issues (the other lanes wait at the end), so the loop
+    // costs as few issue slots as possible on the sub-partition it shares
+    // with softmax and producer warps.
+    if (leader && ok) {
+      int64_t nS[2] = {0, 0}, nP[2] = {0, 0};
+      long long last = clock64();
+      while (nP[0] < nt || nP[1] < nt) {
+        bool did = false;
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const int64_t n = nS[g];
-        if (n < nt && nP[g] == n) {
-          bool rdy = false;
-          if (leader) rdy = bar_test(k_ready, (uint32_t)(n & 1));
-          if (__shfl_sync(0xffffffffu, rdy, 0)) {
+        for (int g = 0; g < 2; ++g) {
+          const int64_t n = nS[g];
+          if (n < nt && nP[g] == n && bar_test(k_ready, (uint32_t)(n & 1))) {
             fence_after();
-            if (leader) {
-              const uint32_t d = tmem + 128u * g, qa = qs + 32768u * g;
+            const uint32_t d = tmem + 128u * g, qa = qs + 32768u * g;
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-                mma_ss(d, desc_sw128(qa + ko), desc_sw128(kh + ko), kIdescQK, j > 0);
-              }
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-                mma_ss(d, desc_sw128(qa + ko), desc_sw128(kl + ko), kIdescQK, 1);
-              }
-              if constexpr (RP > 0) {
-                const uint32_t zh = zs + 2u * g * kZBytes, zl = zh + kZBytes;
-#pragma unroll
-                for (int kk = 0; kk < RP / 16; ++kk) {
-                  mma_ss(d, desc_none(zh + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
-                  mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
-                }
-              }
-              commit(&s_done[g]);
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+              mma_ss(d, desc_sw128(qa + ko), desc_sw128(kh + ko), kIdescQK, j > 0);
             }
-            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+              mma_ss(d, desc_sw128(qa + ko), desc_sw128(kl + ko), kIdescQK, 1);
+            }
+            if constexpr (RP > 0) {
+              const uint32_t zh = zs + 2u * g * kZBytes, zl = zh + kZBytes;
+#pragma unroll
+              for (int kk = 0; kk < RP / 16; ++kk) {
+                mma_ss(d, desc_none(zh + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
+                mma_ss(d, desc_none(zl + 256 * kk, 128, kSbo), desc_none(ea + 256 * kk, 128, kSbo), kIdescF16, 1);
+              }
+            }
+            commit(&s_done[g]);
             ++nS[g];
             did = true;
           }
         }
-      }
 #pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const int64_t n = nP[g];
-        if (n < nS[g]) {
-          bool rdy = false;
-          if (leader) rdy = bar_test(&p_ready[g], (uint32_t)(n & 1)) && bar_test(v_ready, (uint32_t)(n & 1));
-          if (__shfl_sync(0xffffffffu, rdy, 0)) {
+        for (int g = 0; g < 2; ++g) {
+          const int64_t n = nP[g];
+          if (n < nS[g] && bar_test(&p_ready[g], (uint32_t)(n & 1)) && bar_test(v_ready, (uint32_t)(n & 1))) {
             fence_after();
-            if (leader) {
-              const uint32_t ps = tmem + 128u * g;
+            const uint32_t ps = tmem + 128u * g;
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                mma_ts(tmem + kColOa + 128u * g, ps + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
-                       (n > 0 || j > 0) ? 1u : 0u);
-              commit(&pv_done[g]);
-            }
-            __syncwarp();
+            for (int j = 0; j < 8; ++j)
+              mma_ts(tmem + kColOa + 128u * g, ps + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
+                     (n > 0 || j > 0) ? 1u : 0u);
+            commit(&pv_done[g]);
             ++nP[g];
             did = true;
           }
         }
-      }
-      if (did) {
-        last = clock64();
-      } else if (abort_sh) {
-        ok = false;
-      } else if (clock64() - last > kWaitCycles) {
-        if (leader) {
+        if (did) {
+          last = clock64();
+        } else if (abort_sh) {
+          ok = false;
+          break;
+        } else if (clock64() - last > kWaitCycles) {
           abort_sh = 1;
           atomicOr(a.status, kDevTimeout);
+          ok = false;
+          break;
         }
-        ok = false;
       }
-      ok = warp_all(ok);
+      // the last PVs complete before the TMEM is released (bounded)
+      if (ok && nt > 0) {
+        bar_wait(&pv_done[0], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+        bar_wait(&pv_done[1], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+      }
     }
-    // the last PVs complete before the TMEM is released (bounded)
-    if (ok && nt > 0) {
-      bar_wait(&pv_done[0], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
-      bar_wait(&pv_done[1], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
-    }
+    __syncwarp();
   }
 
   fence_before();
