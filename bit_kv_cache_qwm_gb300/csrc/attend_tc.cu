@@ -189,6 +189,46 @@ __device__ __forceinline__ float2 codes_at(uint32_t n) {
   const float2 m = make_float2(__uint_as_float((n & (3u << P)) | e0), __uint_as_float((n & (12u << P)) | e1));
   return __fadd2_rn(m, make_float2(-__uint_as_float(e0), -__uint_as_float(e1)));
 }
+// k_hat as two bf16 terms: hi = k_hat with the low 16 bits of its float32
+// pattern cleared (the truncation to 8 significant bits, exactly a bf16),
+// lo = the remainder k_hat - hi (exact in float32, below one bf16 ulp of hi)
+// rounded to bf16; |k_hat - hi - lo| < 2^-16 |k_hat|.  The hi pair is one
+// byte permute of the two float32 patterns.
+__device__ __forceinline__ void split_bf16x2(float2 kv, uint32_t& hi, uint32_t& lo) {
+  const float2 ht = make_float2(__uint_as_float(__float_as_uint(kv.x) & 0xffff0000u),
+                                __uint_as_float(__float_as_uint(kv.y) & 0xffff0000u));
+  const float2 rem = __fadd2_rn(kv, make_float2(-ht.x, -ht.y));
+  const __nv_bfloat162 lb = __floats2bfloat162_rn(rem.x, rem.y);
+  hi = __byte_perm(__float_as_uint(kv.x), __float_as_uint(kv.y), 0x7632);
+  lo = *reinterpret_cast<const uint32_t*>(&lb);
+}
+// The e row of `key` (r fp16 coefficients, zero-padded to RP) into the
+// no-swizzle K-major core-matrix layout of the PSAC B operand.  With r == RP
+// the rows are 16-byte aligned in the packed tile and copy as vectors.
+template <int RP>
+__device__ __forceinline__ void store_e_row(const uint8_t* e_base, int key, int r, uint8_t* Es) {
+  const __half* esrc = reinterpret_cast<const __half*>(e_base) + key * r;
+  uint8_t* dst = Es + (key >> 3) * (RP / 8) * 128 + (key & 7) * 16;
+  if (r == RP) {
+#pragma unroll
+    for (int j = 0; j < RP / 8; ++j)
+      *reinterpret_cast<uint4*>(dst + j * 128) = reinterpret_cast<const uint4*>(esrc)[j];
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < RP / 8; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int m0 = 8 * j + 2 * e;
+      const __half e0 = m0 < r ? esrc[m0] : __float2half_rn(0.f);
+      const __half e1 = m0 + 1 < r ? esrc[m0 + 1] : __float2half_rn(0.f);
+      const __half2 ee = __halves2half2(e0, e1);
+      w[e] = *reinterpret_cast<const uint32_t*>(&ee);
+    }
+    *reinterpret_cast<uint4*>(dst + j * 128) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -524,36 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
               const float2 rq = __ffma2_rn(cd, ks2, kz2);                      // zero + code*scale
               const float2 cc = make_float2(__uint_as_float(cw[e2] << 16), __uint_as_float(cw[e2] & 0xffff0000u));
               const float2 kv = __fadd2_rn(cc, rq);                            // + centroid
-              const __nv_bfloat162 hb = __floats2bfloat162_rn(kv.x, kv.y);
-              const float2 hf = __bfloat1622float2(hb);
-              const float2 lo = __fadd2_rn(kv, make_float2(-hf.x, -hf.y));
-              const __nv_bfloat162 lb = __floats2bfloat162_rn(lo.x, lo.y);
-              ph[e2] = *reinterpret_cast<const uint32_t*>(&hb);
-              pl[e2] = *reinterpret_cast<const uint32_t*>(&lb);
+              split_bf16x2(kv, ph[e2], pl[e2]);
             }
             const int off = sw128_off(key, chunk);
             *reinterpret_cast<uint4*>(Khi + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
             *reinterpret_cast<uint4*>(Klo + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
           }
           if constexpr (RP > 0) {
-            if (p < 64) {
-              const int ek = hk * 64 + p;
-              const __half* esrc = reinterpret_cast<const __half*>(tb + a.off.e) + ek * a.r;
-#pragma unroll
-              for (int j = 0; j < RP / 8; ++j) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int m0 = 8 * j + 2 * e;
-                  const __half e0 = m0 < a.r ? esrc[m0] : __float2half_rn(0.f);
-                  const __half e1 = m0 + 1 < a.r ? esrc[m0 + 1] : __float2half_rn(0.f);
-                  const __half2 ee = __halves2half2(e0, e1);
-                  w[e] = *reinterpret_cast<const uint32_t*>(&ee);
-                }
-                *reinterpret_cast<uint4*>(Es + ((ek >> 3) * (RP / 8) + j) * 128 + (ek & 7) * 16) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
-              }
-            }
+            if (p < 64) store_e_row<RP>(tb + a.off.e, hk * 64 + p, a.r, Es);
           }
         }
         fence_async_smem();
@@ -609,20 +627,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
     ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
     fence_after();
     // Issue whatever is ready, in tile order per stream: S(t) first half,
-    // S(t) second half, O += P(t) V(t).  Readiness is probed without
-    // blocking (lane 0 probes, the warp follows its answer).
-    int64_t nA = 0, nB = 0, nP = 0;
-    long long last = clock64();
-    while (ok && nP < nt) {
-      bool did = false;
-      if (nA < nt) {
-        const int b = (int)(nA & 1);
-        bool rdy = false;
-        if (leader) rdy = bar_test(kA_ready, (uint32_t)(nA & 1)) && bar_test(kB_ready, (uint32_t)(nA & 1)) &&
-                          (nA < 2 || bar_test(&s_free[b], (uint32_t)(((nA >> 1) - 1) & 1)));
-        if (__shfl_sync(0xffffffffu, rdy, 0)) {
-          fence_after();
-          if (leader) {
+    // S(t) second half, O += P(t) V(t).  The leader alone probes readiness
+    // without blocking and issues; the other lanes wait at the end.
+    if (leader && ok) {
+      int64_t nA = 0, nB = 0, nP = 0;
+      long long last = clock64();
+      while (nP < nt) {
+        bool did = false;
+        if (nA < nt) {
+          const int b = (int)(nA & 1);
+          if (bar_test(kA_ready, (uint32_t)(nA & 1)) && bar_test(kB_ready, (uint32_t)(nA & 1)) &&
+              (nA < 2 || bar_test(&s_free[b], (uint32_t)(((nA >> 1) - 1) & 1)))) {
+            fence_after();
             // full N = 128 MMAs: N = 64 halves run at a fraction of the rate
             const uint32_t d = tmem + kColS0 + 128u * b;
 #pragma unroll
@@ -644,45 +660,37 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
             }
             commit(&sA_done[b]);
             commit(&sB_done[b]);
+            ++nA;
+            ++nB;
+            did = true;
           }
-          __syncwarp();
-          ++nA;
-          ++nB;
-          did = true;
         }
-      }
-      if (nP < nB) {
-        bool rdy = false;
-        if (leader) rdy = bar_test(p_ready, (uint32_t)(nP & 1)) && bar_test(v_ready, (uint32_t)(nP & 1));
-        if (__shfl_sync(0xffffffffu, rdy, 0)) {
+        if (nP < nB && bar_test(p_ready, (uint32_t)(nP & 1)) && bar_test(v_ready, (uint32_t)(nP & 1))) {
           fence_after();
-          if (leader) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              mma_ts(tmem + kColO, tmem + kColP + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
-                     (nP > 0 || j > 0) ? 1u : 0u);
-            commit(pv_done);
-          }
-          __syncwarp();
+          for (int j = 0; j < 8; ++j)
+            mma_ts(tmem + kColO, tmem + kColP + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
+                   (nP > 0 || j > 0) ? 1u : 0u);
+          commit(pv_done);
           ++nP;
           did = true;
         }
-      }
-      if (did) {
-        last = clock64();
-      } else if (abort_sh) {
-        ok = false;
-      } else if (clock64() - last > kWaitCycles) {
-        if (leader) {
+        if (did) {
+          last = clock64();
+        } else if (abort_sh) {
+          ok = false;
+          break;
+        } else if (clock64() - last > kWaitCycles) {
           abort_sh = 1;
           atomicOr(a.status, kDevTimeout);
+          ok = false;
+          break;
         }
-        ok = false;
       }
-      ok = warp_all(ok);
+      // wait for the last PV before the TMEM can be released (bounded)
+      if (ok && nt > 0) bar_wait(pv_done, (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
     }
-    // wait for the last PV before the TMEM can be released (bounded)
-    if (ok && nt > 0) bar_wait(pv_done, (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+    __syncwarp();
   }
 
   fence_before();
@@ -1004,12 +1012,7 @@ __global__ void __launch_bounds__(kThreads2, 1) attend_tc2_kernel(const TcArgs a
           for (int e2 = 0; e2 < 4; ++e2) {
             const float2 rq = __ffma2_rn(cds[e2], ks2, kz2);                 // zero + code*scale
             const float2 kv = __fadd2_rn(cc4[e2], rq);                       // + centroid
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(kv.x, kv.y);
-            const float2 hf = __bfloat1622float2(hb);
-            const float2 lo = __fadd2_rn(kv, make_float2(-hf.x, -hf.y));
-            const __nv_bfloat162 lb = __floats2bfloat162_rn(lo.x, lo.y);
-            ph[e2] = *reinterpret_cast<const uint32_t*>(&hb);
-            pl[e2] = *reinterpret_cast<const uint32_t*>(&lb);
+            split_bf16x2(kv, ph[e2], pl[e2]);
           }
           const int off = sw128_off(key, chunk);
           *reinterpret_cast<uint4*>(Khi + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
@@ -1019,21 +1022,7 @@ __global__ void __launch_bounds__(kThreads2, 1) attend_tc2_kernel(const TcArgs a
       if constexpr (RP > 0) {
         if (p < 128) {
           // e rows: thread = key
-          const __half* esrc = reinterpret_cast<const __half*>(tb + a.off.e) + p * a.r;
-#pragma unroll
-          for (int j = 0; j < RP / 8; ++j) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int m0 = 8 * j + 2 * e;
-              const __half e0 = m0 < a.r ? esrc[m0] : __float2half_rn(0.f);
-              const __half e1 = m0 + 1 < a.r ? esrc[m0 + 1] : __float2half_rn(0.f);
-              const __half2 ee = __halves2half2(e0, e1);
-              w[e] = *reinterpret_cast<const uint32_t*>(&ee);
-            }
-            *reinterpret_cast<uint4*>(Es + ((p >> 3) * (RP / 8) + j) * 128 + (p & 7) * 16) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
+          store_e_row<RP>(tb + a.off.e, p, a.r, Es);
         }
       }
       fence_async_smem();
