@@ -14,6 +14,17 @@
 // fp16, on the tensor cores (mma.sync m16n8k16, float32 accumulation): one
 // product per 32-channel group, scaled afterwards by that key's group scale.
 //
+// Channel orders.  In a packed code word (16 channels, channel c at bits
+// 2c..2c+1) channels c and c+8 lie 16 bits apart, so one shift and one mask
+// put their codes into the two fp16 halves of a register.  The k slots of
+// every m16n8k16 step are therefore filled with channel pairs (c, c+8): slots
+// (2t, 2t+1) hold channels (t, t+8) and slots (2t+8, 2t+9) channels (t+4,
+// t+12) of the step's 16 channels, for Q's A fragments and the codes' B
+// fragments alike (a sum over k does not depend on the order of k).  v_hat
+// is stored with the same pairing along its 128 columns (physical columns
+// 16b+2i, 16b+2i+1 hold dims 16b+i, 16b+i+8), so O comes out of the PV
+// product in that column order and is put back in order when written.
+//
 // Kernels (one head h, one block of 16 query rows mb):
 //   qc_kernel         QC[row][j] = q_row . C[j] for every centroid (bf16
 //                     operands, exact products, float32 sums) into the
@@ -76,11 +87,11 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// two 2-bit codes (bits 0-1, 2-3 of n) as an exact fp16 pair: 1024 + c is
-// exact in fp16 (0x6400 | c)
-__device__ __forceinline__ uint32_t codes_h2u(uint32_t n) {
-  const uint32_t w = 0x64006400u | (n & 3u) | (((n >> 2) & 3u) << 16);
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&w), __float2half2_rn(1024.f));
+// the codes at bits 0-1 and 16-17 of w as an exact fp16 pair (low, high
+// half): 1024 + c is exact in fp16 (0x6400 | c), minus 1024
+__device__ __forceinline__ uint32_t codes_pair16(uint32_t w) {
+  const uint32_t m = (w & 0x00030003u) | 0x64006400u;
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&m), __float2half2_rn(1024.f));
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 // byte offset of element (row, col) of a [rows][128] fp16 tile with a 16-byte
@@ -219,14 +230,17 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
   const __nv_bfloat16* q1 = a.Q + ((int64_t)h * a.M + r1) * kD;
   uint32_t qf[8][4];
   float qsum[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  auto qpair = [&](const __nv_bfloat16* qr, bool in, int c) {   // channels (c, c+8)
+    return in ? make_float2(__bfloat162float(qr[c]), __bfloat162float(qr[c + 8])) : make_float2(0.f, 0.f);
+  };
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    const int c = 16 * ks + 2 * t;
+    const int c = 16 * ks + t;
     float2 x[4];
-    x[0] = r0 < a.M ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q0 + c)) : make_float2(0.f, 0.f);
-    x[1] = r1 < a.M ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q1 + c)) : make_float2(0.f, 0.f);
-    x[2] = r0 < a.M ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q0 + c + 8)) : make_float2(0.f, 0.f);
-    x[3] = r1 < a.M ? __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q1 + c + 8)) : make_float2(0.f, 0.f);
+    x[0] = qpair(q0, r0 < a.M, c);
+    x[1] = qpair(q1, r1 < a.M, c);
+    x[2] = qpair(q0, r0 < a.M, c + 4);
+    x[3] = qpair(q1, r1 < a.M, c + 4);
 #pragma unroll
     for (int i = 0; i < 4; ++i) qf[ks][i] = pack_f16(x[i].x, x[i].y);
     qsum[0][ks >> 1] += (x[0].x + x[0].y) + (x[2].x + x[2].y);
@@ -310,14 +324,10 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
         sg[grp][0] = sg[grp][1] = sg[grp][2] = sg[grp][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
-          // channels 32grp + 16ks + {2t, 2t+1} and {2t+8, 2t+9}: bytes
-          // + 4ks + t/2 and that + 2, nibble t & 1
-          // 8grp + 4ks + t/2 and that + 2, nibble t & 1: both in word 2grp + ks,
-          // at bits 4t and 16 + 4t
-          const uint32_t wv = cw[2 * grp + ks];
-          const uint32_t n0 = (wv >> (4 * t)) & 0xFu;
-          const uint32_t n1 = (wv >> (16 + 4 * t)) & 0xFu;
-          mma_f16(sg[grp], qf[2 * grp + ks], codes_h2u(n0), codes_h2u(n1));
+          // channels 32grp + 16ks + (t, t+8) and (t+4, t+12): word 2grp + ks
+          // shifted by 2t, bits 0/16 and 8/24
+          const uint32_t wv = cw[2 * grp + ks] >> (2 * t);
+          mma_f16(sg[grp], qf[2 * grp + ks], codes_pair16(wv), codes_pair16(wv >> 8));
         }
       }
       float se[4] = {0.f, 0.f, 0.f, 0.f};
@@ -326,10 +336,17 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
 #pragma unroll
         for (int ks = 0; ks < RP / 16; ++ks) {
           const int c = 16 * ks + 2 * t;
-          const __half zero = __float2half_rn(0.f);
-          const __half2 e0 = __halves2half2(c < a.r ? erow[c] : zero, c + 1 < a.r ? erow[c + 1] : zero);
-          const __half2 e1 = __halves2half2(c + 8 < a.r ? erow[c + 8] : zero, c + 9 < a.r ? erow[c + 9] : zero);
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&e0), b1 = *reinterpret_cast<const uint32_t*>(&e1);
+          uint32_t b0, b1;
+          if (a.r == RP) {   // 4-byte aligned pairs
+            b0 = *reinterpret_cast<const uint32_t*>(erow + c);
+            b1 = *reinterpret_cast<const uint32_t*>(erow + c + 8);
+          } else {
+            const __half zero = __float2half_rn(0.f);
+            const __half2 e0 = __halves2half2(c < a.r ? erow[c] : zero, c + 1 < a.r ? erow[c + 1] : zero);
+            const __half2 e1 = __halves2half2(c + 8 < a.r ? erow[c + 8] : zero, c + 9 < a.r ? erow[c + 9] : zero);
+            b0 = *reinterpret_cast<const uint32_t*>(&e0);
+            b1 = *reinterpret_cast<const uint32_t*>(&e1);
+          }
           mma_f16(se, zf[0][ks], b0, b1);
           mma_f16(se, zf[1][ks], b0, b1);
         }
@@ -361,22 +378,34 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
       mx[0] = fmaxf(mx[0], fmaxf(lg[j][0], lg[j][1]));
       mx[1] = fmaxf(mx[1], fmaxf(lg[j][2], lg[j][3]));
     }
+    // lazy rescale: a row's reference maximum moves only when the tile's
+    // maximum exceeds it by more than 2^8 (P <= 2^8 stays within fp16), so O
+    // is rescaled on few tiles
     float mref[2];
+    bool need[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
       mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
       const float mnew = fmaxf(m_run[i], mx[i] * c2);
-      mref[i] = mnew == -INFINITY ? 0.f : mnew;
-      const float corr = m_run[i] == -INFINITY ? 0.f : ex2(m_run[i] - mref[i]);
-      l_run[i] *= corr;
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        o[jj][2 * i] *= corr;
-        o[jj][2 * i + 1] *= corr;
-      }
-      m_run[i] = mnew;
+      need[i] = mnew > m_run[i] + 8.f;       // also when m_run is -inf and mnew finite
     }
+    if (__any_sync(0xffffffffu, need[0] || need[1])) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float mnew = fmaxf(m_run[i], mx[i] * c2);
+        const float corr = !need[i] ? 1.f : (m_run[i] == -INFINITY ? 0.f : ex2(m_run[i] - mnew));
+        l_run[i] *= corr;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          o[jj][2 * i] *= corr;
+          o[jj][2 * i + 1] *= corr;
+        }
+        if (need[i]) m_run[i] = mnew;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) mref[i] = m_run[i] == -INFINITY ? 0.f : m_run[i];
     uint32_t pf[2][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -404,17 +433,20 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
         const __half2 vz2 = __half2half2(__ushort_as_half((unsigned short)(qw[grp] & 0xffffu)));
         const __half2 vs2 = __half2half2(__ushort_as_half((unsigned short)(qw[grp] >> 16)));
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-          const int chunk = grp * 4 + c8;               // 8 channels
-          const uint32_t bits = (vw4[chunk >> 1] >> (16 * (chunk & 1))) & 0xffffu;
-          uint32_t w[4];
+        for (int b2 = 0; b2 < 2; ++b2) {
+          // 16-dim block b = 2grp + b2: physical columns 16b + 2i, 16b + 2i + 1
+          // hold dims 16b + i and 16b + i + 8 (codes at bits 2i and 2i + 16)
+          const int b = 2 * grp + b2;
+          const uint32_t wv = vw4[b];
+          uint32_t w[8];
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const uint32_t cu = codes_h2u(bits >> (4 * e2));
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t cu = codes_pair16(wv >> (2 * i));
             const __half2 hh = __hfma2(*reinterpret_cast<const __half2*>(&cu), vs2, vz2);   // zero + code*scale
-            w[e2] = *reinterpret_cast<const uint32_t*>(&hh);
+            w[i] = *reinterpret_cast<const uint32_t*>(&hh);
           }
-          *reinterpret_cast<uint4*>(vw + swz(lane, 8 * chunk)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(vw + swz(lane, 16 * b)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(vw + swz(lane, 16 * b + 8)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
     }
@@ -458,8 +490,12 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
   float* rw = red + warp * 16 * kPartLd;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    *reinterpret_cast<float2*>(rw + g * kPartLd + 8 * j + 2 * t) = make_float2(o[j][0], o[j][1]);
-    *reinterpret_cast<float2*>(rw + (g + 8) * kPartLd + 8 * j + 2 * t) = make_float2(o[j][2], o[j][3]);
+    // physical columns 8j + 2t, 8j + 2t + 1: dims d and d + 8 of block j / 2
+    const int d = 16 * (j >> 1) + 4 * (j & 1) + t;
+    rw[g * kPartLd + d] = o[j][0];
+    rw[g * kPartLd + d + 8] = o[j][1];
+    rw[(g + 8) * kPartLd + d] = o[j][2];
+    rw[(g + 8) * kPartLd + d + 8] = o[j][3];
   }
   if (t == 0) {
     rw[g * kPartLd + 128] = m_run[0];
@@ -542,26 +578,49 @@ size_t small_smem(const qwm_ctx* c) {
   return 2 * (size_t)c->lay.tile_bytes + kSmallWarps * 8192 + 16 * (size_t)nCp * 4 + 16 * 32 * 4;
 }
 
-// splits per row block: enough CTAs for about 4 per SM, at least 2 tiles each,
-// row blocks x splits <= kMaxParts
-int small_splits(const qwm_ctx* c, int n_mb) {
-  int dev = 0, sms = 152;
+// splits per row block: among 2, 3 or 4 waves of the resident CTA slots (SMs x
+// CTAs per SM, from the occupancy of the kernel instance), the split count
+// whose CTAs fill their waves best (the fewest waves on a tie); at least 2
+// tiles per split and row blocks x splits <= kMaxParts
+int small_splits(const qwm_ctx* c, int n_mb, const void* kern, size_t smem) {
+  int dev = 0, sms = 152, per_sm = 2;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (4LL * sms + (int64_t)c->cfg.heads * n_mb - 1) / ((int64_t)c->cfg.heads * n_mb);
-  int64_t s = want;
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSmallThreads, smem) == cudaSuccess && occ > 0)
+    per_sm = occ;
+  const int64_t units = (int64_t)c->cfg.heads * n_mb, slots = (int64_t)sms * per_sm;
   const int64_t by_tiles = c->n_tiles / 2 > 0 ? c->n_tiles / 2 : 1;
-  if (s > by_tiles) s = by_tiles;
-  if (s > kMaxParts / n_mb) s = kMaxParts / n_mb;
-  return s < 1 ? 1 : (int)s;
+  const int64_t cap = by_tiles < kMaxParts / n_mb ? by_tiles : kMaxParts / n_mb;
+  int64_t best = 1;
+  double best_fill = -1.0;
+  for (int waves = 2; waves <= 4; ++waves) {
+    int64_t s = waves * slots / units;
+    if (s > cap) s = cap;
+    if (s < 1) s = 1;
+    const int64_t ctas = s * units, used = (ctas + slots - 1) / slots;
+    const double fill = (double)ctas / (double)(used * slots);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = s;
+    }
+  }
+  return (int)best;
 }
 
 template <int RP>
-cudaError_t launch_small_rp(const qwm_ctx* c, const SmallArgs& a, cudaStream_t st) {
+cudaError_t launch_small_rp(const qwm_ctx* c, SmallArgs& a, cudaStream_t st) {
   const size_t smem = small_smem(c);
   auto kern = attend_small_kernel<RP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  a.n_split = small_splits(c, a.n_mb, reinterpret_cast<const void*>(kern), smem);
+  qc_kernel<<<dim3(a.n_mb, a.H), kSmallThreads, 0, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   kern<<<dim3(a.n_mb, a.n_split, a.H), kSmallThreads, smem, st>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  combine_kernel<<<dim3((unsigned)a.M, a.H), 32, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -600,19 +659,13 @@ cudaError_t launch_attend_small(const qwm_ctx* c, const void* q, int64_t M, floa
   a.r = c->cfg.rank;
   a.ib = c->ib;
   a.n_mb = (int)((M + 15) / 16);
-  a.n_split = small_splits(c, a.n_mb);
+  a.n_split = 1;
   const size_t qc_bytes = (size_t)a.H * kMaxRowBlocks * 16 * a.nCp * 4;
   a.qc = reinterpret_cast<float*>(ws);
   a.part = reinterpret_cast<float*>(ws + ((qc_bytes + 255) & ~size_t(255)));
   a.status = c->status;
-  qc_kernel<<<dim3(a.n_mb, a.H), kSmallThreads, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const int RP = a.r == 0 ? 0 : (a.r <= 16 ? 16 : 32);
-  e = RP == 0 ? launch_small_rp<0>(c, a, st) : RP == 16 ? launch_small_rp<16>(c, a, st) : launch_small_rp<32>(c, a, st);
-  if (e != cudaSuccess) return e;
-  combine_kernel<<<dim3((unsigned)M, a.H), 32, 0, st>>>(a);
-  return cudaGetLastError();
+  return RP == 0 ? launch_small_rp<0>(c, a, st) : RP == 16 ? launch_small_rp<16>(c, a, st) : launch_small_rp<32>(c, a, st);
 }
 
 }  // namespace qwm
