@@ -196,8 +196,11 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
   extern __shared__ __align__(128) uint8_t sm[];
   uint8_t* ring = sm;                                      // [2][TB]
   uint8_t* vs = sm + 2 * TB;                               // [4 warps][32 keys][128] fp16, swizzled
-  float* qcs = reinterpret_cast<float*>(vs + kSmallWarps * 8192);   // [16][nCp]
-  float* zs = qcs + 16 * a.nCp;                            // [16][32]
+  // QC rows with a stride of nCp + 4 floats: the 8 rows a gather reads for
+  // one key then fall into 8 different bank groups
+  const int qld = a.nCp + 4;
+  float* qcs = reinterpret_cast<float*>(vs + kSmallWarps * 8192);   // [16][qld]
+  float* zs = qcs + 16 * qld;                              // [16][32]
   float* red = reinterpret_cast<float*>(sm);               // [4][16][kPartLd], after the loop
   __shared__ __align__(8) uint64_t full[2], empty[2];
   __shared__ int ok_sh;
@@ -222,8 +225,10 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
   }
   // QC rows of this block
   const float* qcg = a.qc + ((int64_t)h * a.n_mb + mb) * 16 * a.nCp;
-  for (int i = tid; i < 16 * a.nCp / 4; i += kSmallThreads)
-    reinterpret_cast<float4*>(qcs)[i] = reinterpret_cast<const float4*>(qcg)[i];
+  for (int i = tid; i < 16 * a.nCp / 4; i += kSmallThreads) {
+    const int row = i / (a.nCp / 4), c4 = i - row * (a.nCp / 4);
+    reinterpret_cast<float4*>(qcs + row * qld)[c4] = reinterpret_cast<const float4*>(qcg)[i];
+  }
   // Q as fp16 A fragments (the code products) and the per-group row sums
   const int64_t r0 = (int64_t)mb * 16 + g, r1 = r0 + 8;
   const __nv_bfloat16* q0 = a.Q + ((int64_t)h * a.M + r0) * kD;
@@ -358,7 +363,7 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
         const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
         const uint4 qp = *reinterpret_cast<const uint4*>(tb + a.off.kqp + key * G * 4);
         const uint32_t qw[4] = {qp.x, qp.y, qp.z, qp.w};
-        float v0 = qcs[g * a.nCp + idx] + se[kk], v1 = qcs[(g + 8) * a.nCp + idx] + se[2 + kk];
+        float v0 = qcs[g * qld + idx] + se[kk], v1 = qcs[(g + 8) * qld + idx] + se[2 + kk];
 #pragma unroll
         for (int grp = 0; grp < 4; ++grp) {
           const float zr = __half2float(__ushort_as_half((unsigned short)(qw[grp] & 0xffffu)));
@@ -575,7 +580,7 @@ __global__ void __launch_bounds__(32) combine_kernel(const SmallArgs a) {
 
 size_t small_smem(const qwm_ctx* c) {
   const int nCp = (c->cfg.n_centroids + 7) & ~7;
-  return 2 * (size_t)c->lay.tile_bytes + kSmallWarps * 8192 + 16 * (size_t)nCp * 4 + 16 * 32 * 4;
+  return 2 * (size_t)c->lay.tile_bytes + kSmallWarps * 8192 + 16 * (size_t)(nCp + 4) * 4 + 16 * 32 * 4;
 }
 
 // splits per row block: among 2, 3 or 4 waves of the resident CTA slots (SMs x
