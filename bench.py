@@ -375,7 +375,7 @@ def run_gpu(args):
 
     if args.warmup > 0:
         pipelined(args.warmup)
-    e2e_step = pipelined(args.steps)
+    e2e_step = max_over_ranks(pipelined(args.steps), dev)
     # the last end-to-end output is the device-timed steps' output (same inputs)
     e2e_same = bool(torch.equal(h_out[(args.steps - 1) & 1], out.cpu()))
     h2d = sum(x.numel() * x.element_size() for x in h_in)
