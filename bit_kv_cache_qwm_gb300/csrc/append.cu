@@ -1,5 +1,10 @@
 // qwm_append: QSAC centroid choice, INT2 quantisation and 2-bit packing of the
-// key residual and of the value, and the PSAC coefficients, fused in one pass.
+// key residual and of the value in one pass (append_kernel), then the PSAC
+// coefficients (append_e_kernel).  The split lets the quantisation, which
+// needs only the group weights of the new calibration, run while the
+// eigen-solver of that calibration still computes the basis the coefficients
+// need; the second kernel rebuilds k - k_hat from the tile's bytes with the
+// same float32 operations the first one used, so e does not depend on it.
 //
 // QuantWM Abstract: QSAC "jointly considers historical Query sensitivity and
 // residual ranges to select INT2-friendly Key centroids"; roboind article,
@@ -115,7 +120,7 @@ template <int D, typename T, bool NEAREST>
 __global__ void __launch_bounds__(kTile * (D / kGroup))
 append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
               const T* __restrict__ cent, int nC, const float* __restrict__ w,
-              const float* __restrict__ U, int r, uint8_t* __restrict__ cache, int64_t max_tiles,
+              uint8_t* __restrict__ cache, int64_t max_tiles,
               TileOffsets off, int64_t tile0, int32_t version, int2* __restrict__ tiles,
               uint32_t* __restrict__ status, int ib) {
   constexpr int G = D / kGroup;
@@ -126,7 +131,6 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
   constexpr int RS = G * GS;             // row start 4 banks apart (conflict-free LDS.128)
   extern __shared__ __align__(16) float smem[];
   float* cs = smem;                      // [CH][G][GS] negated centroids
-  float* us = smem + CH * RS;            // [r][D] PSAC basis rows
 
   const int h = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -142,8 +146,6 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
     for (int i = 0; i < 32; ++i) kx[i] = 0.f;
   }
   const float wg = w[h * G + gi];
-
-  for (int i = threadIdx.x; i < r * D; i += NT) us[i] = U[(int64_t)h * r * D + i];
 
   // ---- QSAC: exhaustive sensitivity-weighted range score ----
   float best = __int_as_float(0x7f800000);
@@ -231,7 +233,7 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
     }
   }
 
-  // ---- residual of the chosen centroid, INT2, PSAC coefficients ----
+  // ---- residual of the chosen centroid, INT2 ----
   float cj[32];
   load32<T>(ch + (int64_t)bj * D + gi * kGroup, cj);
 #pragma unroll
@@ -240,22 +242,9 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
   uint2 kpk;
   float rh[32];
   const uint32_t kqp = quantize32(cj, &kpk, rh, &sat);
-#pragma unroll
-  for (int i = 0; i < 32; ++i) cj[i] = __fsub_rn(cj[i], rh[i]);    // k - k_hat
-  __syncthreads();   // us ready (the centroid loop syncs too, but not when nC == 0)
 
   const int64_t tile = tile0 + blockIdx.x;
   uint8_t* base = cache + ((int64_t)h * max_tiles + tile) * off.bytes;
-  __half* eout = reinterpret_cast<__half*>(base + off.e) + (int64_t)t * r;
-  for (int m = 0; m < r; ++m) {
-    const float* um = us + m * D + gi * kGroup;
-    float p = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) p = fmaf(um[i], cj[i], p);
-    p += __shfl_xor_sync(kFull, p, TPW);
-    if (G == 4) p += __shfl_xor_sync(kFull, p, 2 * TPW);
-    if (gi == (m % G)) eout[m] = valid ? __float2half_rn(p) : __float2half_rn(0.f);
-  }
 
   // ---- value ----
   float vx[32];
@@ -284,24 +273,112 @@ append_kernel(const T* __restrict__ K, const T* __restrict__ V, int64_t n,
   }
 }
 
+// PSAC coefficients of the tiles append_kernel just wrote: thread (token t,
+// group g) as there, k - k_hat rebuilt from the key, the stored centroid
+// index and the stored codes, zero and scale (rho = f32(k - C), k_hat's
+// residual = f32(zero + f32(code * scale)), delta = f32(rho - that): the same
+// operations append_kernel's quantiser performs), then e_m = U_m . delta as a
+// float32 fma chain over the group's 32 channels and a fixed two-shuffle tree
+// over the groups, rounded once to fp16.  Pad slots get 0.
+template <int D, typename T>
+__global__ void __launch_bounds__(kTile * (D / kGroup))
+append_e_kernel(const T* __restrict__ K, int64_t n, const T* __restrict__ cent, int nC,
+                const float* __restrict__ U, int r, uint8_t* __restrict__ cache, int64_t max_tiles,
+                TileOffsets off, int64_t tile0, int ib) {
+  constexpr int G = D / kGroup;
+  constexpr int NT = kTile * G;
+  constexpr int TPW = 32 / G;
+  constexpr int US = kGroup + 4;                // group slices of a basis row 4 banks apart
+  extern __shared__ __align__(16) float us[];   // [r][G][US] PSAC basis rows
+  const int h = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gi = lane / TPW, ti = lane % TPW;
+  const int t = warp * TPW + ti;
+  const int64_t tok = (int64_t)blockIdx.x * kTile + t;
+  const bool valid = tok < n;
+  for (int i = threadIdx.x; i < r * D; i += NT)
+    us[(i / kGroup) * US + (i % kGroup)] = U[(int64_t)h * r * D + i];
+  const int64_t tile = tile0 + blockIdx.x;
+  uint8_t* base = cache + ((int64_t)h * max_tiles + tile) * off.bytes;
+  float kx[32], cj[32];
+  if (valid) load32<T>(K + ((int64_t)h * n + tok) * D + gi * kGroup, kx);
+  else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) kx[i] = 0.f;
+  }
+  const int bj = ib == 1 ? base[off.idx + t] : reinterpret_cast<const uint16_t*>(base + off.idx)[t];
+  load32<T>(cent + ((int64_t)h * nC + bj) * D + gi * kGroup, cj);
+  const uint2 kpk = *reinterpret_cast<const uint2*>(base + off.kcode + t * (D / 4) + gi * 8);
+  const uint32_t kqp = *reinterpret_cast<const uint32_t*>(base + off.kqp + (t * G + gi) * 4);
+  const float zf = __half2float(__ushort_as_half((unsigned short)(kqp & 0xffffu)));
+  const float sf = __half2float(__ushort_as_half((unsigned short)(kqp >> 16)));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t c = ((i < 16 ? kpk.x : kpk.y) >> (2 * (i & 15))) & 3u;
+    const float rho = __fsub_rn(kx[i], cj[i]);
+    cj[i] = __fsub_rn(rho, __fadd_rn(zf, __fmul_rn((float)c, sf)));   // k - k_hat
+  }
+  __syncthreads();   // us ready
+  __half* eout = reinterpret_cast<__half*>(base + off.e) + (int64_t)t * r;
+  for (int m = 0; m < r; ++m) {
+    const float4* um = reinterpret_cast<const float4*>(us + (m * G + gi) * US);
+    float p = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 u4 = um[i];
+      p = fmaf(u4.x, cj[4 * i], p);
+      p = fmaf(u4.y, cj[4 * i + 1], p);
+      p = fmaf(u4.z, cj[4 * i + 2], p);
+      p = fmaf(u4.w, cj[4 * i + 3], p);
+    }
+    p += __shfl_xor_sync(kFull, p, TPW);
+    if (G == 4) p += __shfl_xor_sync(kFull, p, 2 * TPW);
+    if (gi == (m % G)) eout[m] = valid ? __float2half_rn(p) : __float2half_rn(0.f);
+  }
+}
+
+template <int D, typename T>
+cudaError_t launch_e_t(const qwm_ctx* c, const void* k, int64_t n, int64_t tile0, int32_t slot,
+                       cudaStream_t st) {
+  const int r = c->cfg.rank, H = c->cfg.heads;
+  const size_t smem = (size_t)r * (D / kGroup) * (kGroup + 4) * 4;
+  auto kern = append_e_kernel<D, T>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((n + kTile - 1) / kTile), (unsigned)H);
+  const float* U = c->basis + (size_t)slot * H * r * D;
+  kern<<<grid, kTile * (D / kGroup), smem, st>>>((const T*)k, n, (const T*)c->centroids, c->cfg.n_centroids,
+                                                 U, r, c->cache, c->lay.max_tiles, tile_offsets(c->lay), tile0,
+                                                 c->ib);
+  return cudaGetLastError();
+}
+
 template <int D, typename T>
 cudaError_t launch_t(const qwm_ctx* c, const void* k, const void* v, int64_t n, int64_t tile0,
                      int32_t version, cudaStream_t st) {
-  const int r = c->cfg.rank, H = c->cfg.heads, nC = c->cfg.n_centroids;
+  const int H = c->cfg.heads, nC = c->cfg.n_centroids;
   constexpr int CH = 16384 / D;
-  const size_t smem = (size_t)CH * (D / kGroup) * (kGroup + 4) * 4 + (size_t)r * D * 4;
+  const size_t smem = (size_t)CH * (D / kGroup) * (kGroup + 4) * 4;
   auto kern = c->assign == 1 ? append_kernel<D, T, true> : append_kernel<D, T, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((n + kTile - 1) / kTile), (unsigned)H);
-  const float* U = c->basis + (size_t)version * H * r * D;   // version = basis slot
   kern<<<grid, kTile * (D / kGroup), smem, st>>>(
-      (const T*)k, (const T*)v, n, (const T*)c->centroids, nC, c->w, U, r, c->cache,
+      (const T*)k, (const T*)v, n, (const T*)c->centroids, nC, c->w, c->cache,
       c->lay.max_tiles, tile_offsets(c->lay), tile0, version, c->tiles, c->status, c->ib);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_append_e(const qwm_ctx* c, const void* k, int64_t n, int64_t tile0, int32_t slot,
+                            cudaStream_t st) {
+  if (c->cfg.rank == 0) return cudaSuccess;
+  const bool bf = c->cfg.dtype == QWM_BF16;
+  if (c->cfg.head_dim == 128)
+    return bf ? launch_e_t<128, __nv_bfloat16>(c, k, n, tile0, slot, st) : launch_e_t<128, float>(c, k, n, tile0, slot, st);
+  return bf ? launch_e_t<64, __nv_bfloat16>(c, k, n, tile0, slot, st) : launch_e_t<64, float>(c, k, n, tile0, slot, st);
+}
 
 cudaError_t launch_append(const qwm_ctx* c, const void* k, const void* v, int64_t n, int64_t tile0,
                           int32_t version, cudaStream_t st) {

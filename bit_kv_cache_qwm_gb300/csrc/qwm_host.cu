@@ -31,6 +31,21 @@ cudaStream_t S(void* p) { return reinterpret_cast<cudaStream_t>(p); }
 
 qwm_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QWM_OK : QWM_ERR_CUDA; }
 
+// The caller's stream waits for the eigen-solver of the last calibration (a
+// no-op once it has finished).
+cudaError_t join_eig(const qwm_ctx* x, cudaStream_t s) {
+  return x->eig_pending ? cudaStreamWaitEvent(s, x->ev_eig, 0) : cudaSuccess;
+}
+
+void release_streams(qwm_ctx* x) {
+  if (x->side) cudaStreamSynchronize(x->side);
+  if (x->ev_fork) cudaEventDestroy(x->ev_fork);
+  if (x->ev_eig) cudaEventDestroy(x->ev_eig);
+  if (x->side) cudaStreamDestroy(x->side);
+  x->side = nullptr;
+  x->ev_fork = x->ev_eig = nullptr;
+}
+
 }  // namespace
 
 extern "C" const char* qwm_status_string(qwm_status s) {
@@ -130,8 +145,16 @@ extern "C" qwm_status qwm_create(const qwm_config* c, void* d_cache, void* d_sta
   x->centroids_set = false;
   x->attend_kernel = 0;
   x->assign = 0;
+  // the eigen-solver's stream has the highest priority: its few CTAs are
+  // dispatched before those of the quantisation that becomes ready with it
+  int lo_prio = 0, hi_prio = 0;
   if (cudaMemset(d_state, 0, L.state_bytes) != cudaSuccess ||
-      cudaDeviceSynchronize() != cudaSuccess) {
+      cudaDeviceSynchronize() != cudaSuccess ||
+      cudaDeviceGetStreamPriorityRange(&lo_prio, &hi_prio) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&x->side, cudaStreamNonBlocking, hi_prio) != cudaSuccess ||
+      cudaEventCreateWithFlags(&x->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&x->ev_eig, cudaEventDisableTiming) != cudaSuccess) {
+    release_streams(x);
     delete x;
     return QWM_ERR_CUDA;
   }
@@ -140,6 +163,7 @@ extern "C" qwm_status qwm_create(const qwm_config* c, void* d_cache, void* d_sta
 }
 
 extern "C" qwm_status qwm_destroy(qwm_ctx* ctx) {
+  if (ctx) release_streams(ctx);
   delete ctx;
   return QWM_OK;
 }
@@ -187,10 +211,19 @@ extern "C" qwm_status qwm_calibrate(qwm_ctx* x, const void* d_q, int64_t n_h, vo
   int32_t v, slot;
   qwm_status st = next_version(x, &v, &slot);
   if (st != QWM_OK) return st;
-  cudaError_t e = launch_gram(x, d_q, n_h, S(stream));
-  if (e == cudaSuccess) e = launch_eig(x, n_h, slot, S(stream));
-  if (e == cudaSuccess) e = launch_group_weights(x, S(stream));
+  // Gram sums on the caller's stream (after the previous eigen-solver has
+  // read the partial sums this overwrites), then the eigen-solver on the side
+  // stream and the group weights on the caller's
+  cudaStream_t s = S(stream);
+  cudaError_t e = join_eig(x, s);
+  if (e == cudaSuccess) e = launch_gram(x, d_q, n_h, s);
+  if (e == cudaSuccess) e = cudaEventRecord(x->ev_fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(x->side, x->ev_fork, 0);
+  if (e == cudaSuccess) e = launch_eig(x, n_h, slot, x->side);
+  if (e == cudaSuccess) e = cudaEventRecord(x->ev_eig, x->side);
+  if (e == cudaSuccess) e = launch_group_weights(x, s);
   if (e != cudaSuccess) return QWM_ERR_CUDA;
+  x->eig_pending = true;
   x->version = v;
   x->slot = slot;
   return QWM_OK;
@@ -204,7 +237,8 @@ extern "C" qwm_status qwm_set_calibration(qwm_ctx* x, const float* h_s, const fl
   if (st != QWM_OK) return st;
   const size_t H = x->cfg.heads, d = x->cfg.head_dim, r = x->cfg.rank;
   cudaStream_t s = S(stream);
-  cudaError_t e = cudaMemcpyAsync(x->s, h_s, H * d * 4, cudaMemcpyHostToDevice, s);
+  cudaError_t e = join_eig(x, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(x->s, h_s, H * d * 4, cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess && r > 0) {
     float* dst = x->basis + (size_t)slot * H * r * d;
     e = cudaMemcpyAsync(dst, h_U, H * r * d * 4, cudaMemcpyHostToDevice, s);
@@ -225,8 +259,8 @@ extern "C" qwm_status qwm_get_calibration(qwm_ctx* x, float* h_s, float* h_U, fl
   if (x->version < 0) return QWM_ERR_NOT_CALIBRATED;
   const size_t H = x->cfg.heads, d = x->cfg.head_dim, r = x->cfg.rank;
   cudaStream_t s = S(stream);
-  cudaError_t e = cudaSuccess;
-  if (h_s) e = cudaMemcpyAsync(h_s, x->s, H * d * 4, cudaMemcpyDeviceToHost, s);
+  cudaError_t e = join_eig(x, s);
+  if (e == cudaSuccess && h_s) e = cudaMemcpyAsync(h_s, x->s, H * d * 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess && h_U && r > 0)
     e = cudaMemcpyAsync(h_U, x->basis + (size_t)x->slot * H * r * d,
                         H * r * d * 4, cudaMemcpyDeviceToHost, s);
@@ -246,7 +280,12 @@ extern "C" qwm_status qwm_append(qwm_ctx* x, const void* d_k, const void* d_v, i
   if (x->version < 0 || !x->centroids_set) return QWM_ERR_NOT_CALIBRATED;
   const int64_t tiles = (n + kTile - 1) / kTile;
   if (x->n_tiles + tiles > x->lay.max_tiles) return QWM_ERR_CAPACITY;
-  cudaError_t e = launch_append(x, d_k, d_v, n, x->n_tiles, x->slot, S(stream));
+  // quantisation (group weights only), then the PSAC coefficients once the
+  // basis of the current calibration is there
+  cudaStream_t s = S(stream);
+  cudaError_t e = launch_append(x, d_k, d_v, n, x->n_tiles, x->slot, s);
+  if (e == cudaSuccess && x->cfg.rank > 0) e = join_eig(x, s);
+  if (e == cudaSuccess) e = launch_append_e(x, d_k, n, x->n_tiles, x->slot, s);
   if (e != cudaSuccess) return QWM_ERR_CUDA;
   SegmentRec r;
   r.first_tile = x->n_tiles;
@@ -273,11 +312,14 @@ extern "C" qwm_status qwm_attend(qwm_ctx* x, const void* d_q, int64_t M, float s
   if (k == 2 && !attend_mma_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 3 && !attend_tc_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 4 && !attend_tc2_supported(x)) return QWM_ERR_UNSUPPORTED;
-  cudaError_t e = k == 5   ? launch_attend_small(x, d_q, M, scale, d_out, x->ws + small_workspace_offset(x->cfg), S(stream))
-                  : k == 4 ? launch_attend_tc2(x, d_q, M, scale, d_out, S(stream))
-                  : k == 3 ? launch_attend_tc(x, d_q, M, scale, d_out, S(stream))
-                  : k == 2 ? launch_attend_mma(x, d_q, M, scale, d_out, S(stream))
-                           : launch_attend_simt(x, d_q, M, scale, d_out, S(stream));
+  cudaStream_t s = S(stream);
+  cudaError_t e = join_eig(x, s);   // the basis of the last calibration
+  if (e != cudaSuccess) return QWM_ERR_CUDA;
+  e = k == 5   ? launch_attend_small(x, d_q, M, scale, d_out, x->ws + small_workspace_offset(x->cfg), s)
+      : k == 4 ? launch_attend_tc2(x, d_q, M, scale, d_out, s)
+      : k == 3 ? launch_attend_tc(x, d_q, M, scale, d_out, s)
+      : k == 2 ? launch_attend_mma(x, d_q, M, scale, d_out, s)
+               : launch_attend_simt(x, d_q, M, scale, d_out, s);
   return cuda_status(e);
 }
 
@@ -297,7 +339,8 @@ extern "C" qwm_status qwm_peek_status_bits(qwm_ctx* x, uint32_t* bits, void* str
   if (!x || !bits) return QWM_ERR_INVALID_ARG;
   cudaStream_t s = S(stream);
   uint32_t h = 0;
-  cudaError_t e = cudaMemcpyAsync(&h, x->status, 4, cudaMemcpyDeviceToHost, s);
+  cudaError_t e = join_eig(x, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, x->status, 4, cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(x->status, 0, 4, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return QWM_ERR_CUDA;
@@ -323,7 +366,9 @@ extern "C" qwm_status qwm_set_assignment(qwm_ctx* x, int32_t mode) {
 extern "C" qwm_status qwm_dequantize(qwm_ctx* x, float* d_khat, float* d_vhat, float* d_e, void* stream) {
   if (!x || !d_khat || !d_vhat || (x->cfg.rank > 0 && !d_e)) return QWM_ERR_INVALID_ARG;
   if (!x->centroids_set) return QWM_ERR_NOT_CALIBRATED;
-  return cuda_status(launch_dequantize(x, d_khat, d_vhat, d_e, S(stream)));
+  cudaError_t e = join_eig(x, S(stream));
+  if (e == cudaSuccess) e = launch_dequantize(x, d_khat, d_vhat, d_e, S(stream));
+  return cuda_status(e);
 }
 
 extern "C" qwm_status qwm_set_attend_kernel(qwm_ctx* x, int32_t k) {

@@ -55,6 +55,14 @@ struct qwm_ctx {
   int32_t attend_kernel;
   int32_t assign;        // 0 QSAC, 1 nearest centroid
   std::vector<qwm::SegmentRec> segs;
+  // The eigen-solver of a calibration runs on `side`, forked from the
+  // caller's stream after the Gram sums and group weights (ev_fork) and joined
+  // (ev_eig) by every later call that reads the basis, the eigen-solver's
+  // outputs, its workspace or the status word; append's quantisation, which
+  // needs only the group weights, runs before the join.
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_eig = nullptr;
+  bool eig_pending = false;
 };
 
 namespace qwm {
@@ -62,6 +70,8 @@ namespace qwm {
 // ---- launchers (each returns cudaGetLastError() of its launch) ----
 cudaError_t launch_append(const qwm_ctx* c, const void* k, const void* v, int64_t n,
                           int64_t tile0, int32_t version, cudaStream_t st);
+cudaError_t launch_append_e(const qwm_ctx* c, const void* k, int64_t n, int64_t tile0, int32_t slot,
+                            cudaStream_t st);
 cudaError_t launch_gram(const qwm_ctx* c, const void* q, int64_t n_h, cudaStream_t st);
 cudaError_t launch_eig(const qwm_ctx* c, int64_t n_h, int32_t version, cudaStream_t st);
 cudaError_t launch_group_weights(const qwm_ctx* c, cudaStream_t st);

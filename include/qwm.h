@@ -23,7 +23,10 @@
  *     configured dtype (float32 or bfloat16).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Compute calls are asynchronous on that stream; calls on one
- *     context must be ordered (one stream, or events between streams).
+ *     context must be ordered (one stream, or events between streams).  One
+ *     exception: the eigen-solver of qwm_calibrate runs on a stream the
+ *     context owns (see qwm_calibrate); every later call that reads what it
+ *     writes makes its own stream wait for it first.
  *   - Errors found on the host (arguments, sizes, capacity, call order) are
  *     returned before any launch and leave the context unchanged.  A CUDA
  *     launch error returns QWM_ERR_CUDA.  Conditions found on the device (an
@@ -115,7 +118,8 @@ qwm_status qwm_sizes(const qwm_config* cfg, qwm_layout* out);
 qwm_status qwm_create(const qwm_config* cfg, void* d_cache, void* d_state, void* d_workspace,
                       qwm_ctx** out);
 
-/* Release the host handle (device buffers stay with the caller). NULL is a no-op. */
+/* Release the host handle (device buffers stay with the caller); waits for
+ * the context's own stream first.  NULL is a no-op. */
 qwm_status qwm_destroy(qwm_ctx* ctx);
 
 /* Copy the high-precision centroids [H][C][d] (configured dtype, device) into
@@ -132,7 +136,17 @@ qwm_status qwm_set_centroids(qwm_ctx* ctx, const void* d_centroids, void* stream
  * tends to be concentrated in a few directions", roboind article "Step 2").
  * Opens a new basis version: later appends store coefficients in it.
  * Needs 1 <= n_h <= max_hist.  Asynchronous; non-convergence within max_iter
- * sets QWM_DEV_NOT_CONVERGED and keeps the best basis found. */
+ * sets QWM_DEV_NOT_CONVERGED and keeps the best basis found.
+ * Streams: the Gram sums, s and the group weights are computed on `stream`;
+ * the eigen-solver then runs on a stream owned by the context, after them.
+ * Later calls on the context that read its results (the coefficient step of
+ * qwm_append, qwm_attend, qwm_calibrate, qwm_set_calibration,
+ * qwm_get_calibration, qwm_get_status, qwm_peek_status_bits,
+ * qwm_dequantize) make their stream wait for it, so the quantisation of the
+ * next qwm_append, which needs only the group weights, overlaps it.  Code
+ * that reads the basis in the state buffer directly must first issue one of
+ * those calls on its stream.  Under CUDA graph capture, end the capture
+ * after such a call (it joins the context's stream back into the graph). */
 qwm_status qwm_calibrate(qwm_ctx* ctx, const void* d_q_hist, int64_t n_h, void* stream);
 
 /* Calibration for callers that cannot allocate device memory.  (The QuantWM
@@ -185,7 +199,10 @@ qwm_status qwm_get_calibration(qwm_ctx* ctx, float* h_s, float* h_U, float* h_la
  * as r fp16 values (QuantWM Abstract; roboind article "Step 1", "Step 2").
  * Occupies ceil(n/128) new tiles; slots past n in the last tile are zeroed
  * and masked in attention.  n = 0 is a no-op.  Needs a calibration and
- * centroids.  Asynchronous. */
+ * centroids.  Asynchronous: the quantisation runs at once on `stream`, the
+ * coefficients e after the eigen-solver of the last qwm_calibrate (two
+ * kernels; the second rebuilds k - k_hat from the tile with the same float32
+ * operations). */
 qwm_status qwm_append(qwm_ctx* ctx, const void* d_k, const void* d_v, int64_t n, void* stream);
 
 /* Attention of M query rows [H][M][d] over every cached token:

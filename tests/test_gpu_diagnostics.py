@@ -108,14 +108,15 @@ def test_diagnostics_agree_with_oracle(qwm):
     cent = centroids(name, tuple(heads))
     ctx = qwm.Qwm(2, 128, wl.rank, wl.n_centroids, dtype="bf16", max_tokens=2 * 37 * 128, max_hist=wl.n_hist)
     ctx.set_centroids(T(cent))
-    ctx.calibrate(T(synth.hist_queries(wl, 0, heads)))
+    s_, U = calibration(name, tuple(heads))      # the oracle's sensitivity and basis
+    ctx.set_calibration(s_, U)
     for ch in range(2):
         ctx.append(T(ks[ch]), T(vs[ch]))
     K = torch.from_numpy(np.concatenate(ks, axis=1)).to(dev).float()
     V = torch.from_numpy(np.concatenate(vs, axis=1)).to(dev).float()
     qn = synth.queries(wl, 0, heads, m=rows)
     got = diagnostics.measure(ctx, K, V, torch.from_numpy(qn).to(dev).float(), 1 / np.sqrt(128))
-    U = ctx.get_calibration()["U"].astype(np.float64)
+    U = U.astype(np.float64)
     tiles, table = ctx.cache_tiles().cpu().numpy(), ctx.tile_table().cpu().numpy()
     q64, K64, V64 = qn.astype(np.float64), K.double().cpu().numpy(), V.double().cpu().numpy()
     changes, num, den = [], 0.0, 0.0
