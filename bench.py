@@ -412,7 +412,8 @@ def run_gpu(args):
                 "copies": "second stream, double-buffered: inputs of step i+1 and output of step i-1 "
                           "move while step i computes", "output_matches_device_timed": e2e_same},
         # gram, gram sum, A^2, eig, weights, append, attend (A^2 only when r > 0)
-        "gpu_launches": args.steps * (7 if r > 0 else 6),
+        # gram, gram_sum, [square], eig, weights, append, [append_e], attend
+        "gpu_launches": args.steps * (8 if r > 0 else 6),
         "clocks": clk.summary(),
         "wall_s": t_wall,
         "device_status": int(st),
