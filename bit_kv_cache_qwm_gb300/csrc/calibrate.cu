@@ -932,10 +932,15 @@ cudaError_t gram_and_sum(int H, int dtype, const void* q, int64_t n_h, float* pa
 }
 
 template <int D>
-cudaError_t square_and_eig(int H, int r, int m, int max_iter, const float* part, int splits, float* a2, float* gws,
-                           bool use_smem, float* U, float* lam, float* energy, int32_t* iters, uint32_t* status,
-                           cudaStream_t st) {
+cudaError_t square_only(int H, int r, int m, const float* part, int splits, float* a2, cudaStream_t st) {
   if (r > 0 && m < D) square_kernel<D><<<dim3(H, (D / 32) * (D / 32)), 256, 0, st>>>(part, splits, a2);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t eig_only(int H, int r, int m, int max_iter, const float* part, int splits, float* a2, float* gws,
+                     bool use_smem, float* U, float* lam, float* energy, int32_t* iters, uint32_t* status,
+                     cudaStream_t st) {
   const size_t smem = use_smem ? eig_layout(D, m).floats * 4 : 0;
   cudaError_t e = cudaFuncSetAttribute(eig_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -944,12 +949,32 @@ cudaError_t square_and_eig(int H, int r, int m, int max_iter, const float* part,
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t square_and_eig(int H, int r, int m, int max_iter, const float* part, int splits, float* a2, float* gws,
+                           bool use_smem, float* U, float* lam, float* energy, int32_t* iters, uint32_t* status,
+                           cudaStream_t st) {
+  cudaError_t e = square_only<D>(H, r, m, part, splits, a2, st);
+  if (e != cudaSuccess) return e;
+  return eig_only<D>(H, r, m, max_iter, part, splits, a2, gws, use_smem, U, lam, energy, iters, status, st);
+}
+
 cudaError_t launch_gram(const qwm_ctx* c, const void* q, int64_t n_h, cudaStream_t st) {
   const int sp = splits_for(n_h);
   const int64_t rps = (n_h + sp - 1) / sp;
   float* part = (float*)c->ws;
   if (c->cfg.head_dim == 128) return gram_and_sum<128>(c->cfg.heads, c->cfg.dtype, q, n_h, part, sp, rps, c->s, st);
   return gram_and_sum<64>(c->cfg.heads, c->cfg.dtype, q, n_h, part, sp, rps, c->s, st);
+}
+
+cudaError_t launch_square(const qwm_ctx* c, int64_t n_h, cudaStream_t st) {
+  const int D = c->cfg.head_dim, H = c->cfg.heads, r = c->cfg.rank;
+  const int m = eig_cols(c->cfg);
+  const CalibWs w = calib_ws(H, D, m, splits_for(c->cfg.max_hist));
+  const float* part = (const float*)c->ws;
+  float* a2 = (float*)(c->ws + w.a2);
+  const int sp = splits_for(n_h);
+  if (D == 128) return square_only<128>(H, r, m, part, sp, a2, st);
+  return square_only<64>(H, r, m, part, sp, a2, st);
 }
 
 cudaError_t launch_eig(const qwm_ctx* c, int64_t n_h, int32_t version, cudaStream_t st) {
@@ -962,10 +987,10 @@ cudaError_t launch_eig(const qwm_ctx* c, int64_t n_h, int32_t version, cudaStrea
   float* U = c->basis + (size_t)version * H * (r > 0 ? r : 1) * D;   // version = basis slot
   const int sp = splits_for(n_h);
   if (D == 128)
-    return square_and_eig<128>(H, r, m, c->cfg.max_iter, part, sp, a2, gws, w.use_smem, U, c->lambda, c->energy,
-                               c->iters, c->status, st);
-  return square_and_eig<64>(H, r, m, c->cfg.max_iter, part, sp, a2, gws, w.use_smem, U, c->lambda, c->energy,
-                            c->iters, c->status, st);
+    return eig_only<128>(H, r, m, c->cfg.max_iter, part, sp, a2, gws, w.use_smem, U, c->lambda, c->energy,
+                         c->iters, c->status, st);
+  return eig_only<64>(H, r, m, c->cfg.max_iter, part, sp, a2, gws, w.use_smem, U, c->lambda, c->energy,
+                      c->iters, c->status, st);
 }
 
 cudaError_t launch_group_weights(const qwm_ctx* c, cudaStream_t st) {

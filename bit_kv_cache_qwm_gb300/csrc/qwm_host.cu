@@ -211,12 +211,16 @@ extern "C" qwm_status qwm_calibrate(qwm_ctx* x, const void* d_q, int64_t n_h, vo
   int32_t v, slot;
   qwm_status st = next_version(x, &v, &slot);
   if (st != QWM_OK) return st;
-  // Gram sums on the caller's stream (after the previous eigen-solver has
-  // read the partial sums this overwrites), then the eigen-solver on the side
-  // stream and the group weights on the caller's
+  // Gram sums and A^2 on the caller's stream (after the previous
+  // eigen-solver has read the buffers this overwrites), then the eigen-solver
+  // on the side stream and the group weights on the caller's: the
+  // eigen-solver is ready before the quantisation of the next append, so its
+  // CTAs get SMs first (a quantisation CTA and an eigen-solver CTA do not fit
+  // on one SM together)
   cudaStream_t s = S(stream);
   cudaError_t e = join_eig(x, s);
   if (e == cudaSuccess) e = launch_gram(x, d_q, n_h, s);
+  if (e == cudaSuccess) e = launch_square(x, n_h, s);
   if (e == cudaSuccess) e = cudaEventRecord(x->ev_fork, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(x->side, x->ev_fork, 0);
   if (e == cudaSuccess) e = launch_eig(x, n_h, slot, x->side);

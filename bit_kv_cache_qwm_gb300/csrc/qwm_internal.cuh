@@ -73,6 +73,7 @@ cudaError_t launch_append(const qwm_ctx* c, const void* k, const void* v, int64_
 cudaError_t launch_append_e(const qwm_ctx* c, const void* k, int64_t n, int64_t tile0, int32_t slot,
                             cudaStream_t st);
 cudaError_t launch_gram(const qwm_ctx* c, const void* q, int64_t n_h, cudaStream_t st);
+cudaError_t launch_square(const qwm_ctx* c, int64_t n_h, cudaStream_t st);
 cudaError_t launch_eig(const qwm_ctx* c, int64_t n_h, int32_t version, cudaStream_t st);
 cudaError_t launch_group_weights(const qwm_ctx* c, cudaStream_t st);
 cudaError_t launch_dequantize(const qwm_ctx* c, float* khat, float* vhat, float* e, cudaStream_t st);
