@@ -502,7 +502,11 @@ def run_small_m(args):
                    "n_centroids": C, "rank": r, "l2": "flushed between steps (256 MiB write)",
                    "attend_kernel": kern},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "qwm_attend",
+                     "frac": gbs / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic(os.path.join(ROOT, "profiles", f"attend_small_{wl.name}_m{M}.md"),
+                                                 os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc", "attend_small.cu"))
+                     if kern == 5 else None,
+                     "kernel": "qwm_attend",
                      "bytes_per_launch": nbytes, "peak_source": peaks["source"] + " HBM copy"},
         "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": q.numel() * q.element_size(),
