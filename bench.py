@@ -1,19 +1,32 @@
-"""Throughput of the QuantWM 2-bit KV-cache hot path on one GB300 (or N, as
-independent replicas).
+"""Throughput of the QuantWM 2-bit KV-cache hot path on one GB300 (or N).
 
-One step is one pass of the whole path over one chunk of a 12-head video
-world-model cache (21 latent frames of 1,560 tokens held, 3-frame chunks):
-  qwm_calibrate  (1,024 historical queries per head, PSAC rank 16)
+Default workload: the long streaming video world-model cache, 24 heads,
+d = 128, 256 centroids, PSAC rank 16, 240 latent frames of 1,560 tokens held
+(374,400 cached tokens after the step).  The cache is first built as a real
+stream: 79 steps of {qwm_calibrate on the 4,096-query ring of the previous
+chunk, qwm_append of 4,680 tokens}, so it holds 79 segments, each with its
+own PSAC basis version.  One timed step is then the 80th step of the stream:
+  qwm_calibrate  (the 4,096-query ring, PSAC rank 16)
   qwm_append     (4,680 new tokens: QSAC over 256 centroids, INT2, PSAC e)
-  qwm_attend     (4,680 query rows over the 32,760 cached tokens)
-after which the cache is rewound to its 6-chunk prefix (host bookkeeping),
-so every step does the same work.  L2 is flushed between steps.
+  qwm_attend     (the chunk's 4,680 query rows over all 374,400 tokens)
+after which the cache is rewound to its 79-segment prefix (host bookkeeping),
+so every timed step does the same work.  L2 is flushed between steps.
 
 `value` is the attention algorithmic throughput of the whole step,
-H (4 M N d + 2 M N r + 2 M d r) flops per step / step time, in TFLOP/s;
-the kernel-only numbers (attend TFLOP/s and cache GB/s, append Mtokens/s)
-are reported beside it.  `--impl reference` times the fp64 CPU oracle on a
-bounded sample of the same step on the host cores.
+H (4 M N d + 2 M N r + 2 M d r) flops per step / step time, in TFLOP/s.
+`roofline` is the attention kernel's rate against the measured bf16 peak;
+`roofline_append` the append kernels' HBM rate (timed alone, after the main
+loop) against the measured HBM copy bandwidth.
+
+Other modes: `--workload NAME` (any synthetic workload), `--sweep` (the
+append-only sweep: chunk length x centroids x rank, one JSON line per point),
+`--small-m M` (few query rows, cache GB/s), `--only CALL` (profiling runs).
+`--impl reference` times the fp64 CPU oracle on a bounded sample.
+
+With N ranks (torchrun), every rank owns its own shard of heads of an N-times
+larger job (rank i: heads [i H, (i+1) H) of the synthetic stream), so the
+per-GPU work is fixed (weak scaling) and no data crosses ranks; the only
+collectives are a barrier and the max-over-ranks of the step time.
 """
 from __future__ import annotations
 
@@ -26,6 +39,7 @@ import statistics
 import subprocess
 import sys
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -35,15 +49,17 @@ if ROOT not in sys.path:
 
 from bit_kv_cache_qwm_gb300 import synth  # noqa: E402
 
-WORKLOAD = "bf16-h12-n32760"
+WORKLOAD = "bf16-h24-stream-n374400"
 METRIC = "qwm_attend TFLOP/s & cache GB/s (% roofline); qwm_append Mtokens/s"
 L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
+KERNEL_IDS = {"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4}
+KERNEL_NAMES = {0: "auto", 1: "simt", 2: "mma", 3: "tcgen05", 4: "tcgen05-2tile", 5: "few-row"}
 
 
 def profiled_traffic(summary, source):
-    """DRAM bytes (read + write) per launch of the attention kernel from a
-    committed ncu summary, when the summary records the sha256 of the kernel
-    source it was captured on and that source is unchanged; else None."""
+    """DRAM bytes (read + write) per launch of a kernel from a committed ncu
+    summary, when the summary records the sha256 of the kernel source it was
+    captured on and that source is unchanged; else None."""
     try:
         with open(summary) as f:
             text = f.read()
@@ -60,6 +76,19 @@ def attend_flops(H, M, N, d, r):
     return H * (4.0 * M * N * d + 2.0 * M * N * r + 2.0 * M * d * r)
 
 
+def append_bytes_per_token_head(d, bytes_per_token, in_elem=2):
+    """HBM bytes one appended token of one head moves: k and v in, packed out."""
+    return 2 * d * in_elem + bytes_per_token
+
+
+def shard_heads(rank: int, world: int, heads: int) -> list:
+    """Global head indices of `rank`'s shard: every rank owns `heads` heads of
+    a job of world * heads heads (weak scaling; disjoint shards)."""
+    if not (0 <= rank < world) or heads < 1:
+        raise ValueError("rank must lie in [0, world) and heads be positive")
+    return list(range(rank * heads, (rank + 1) * heads))
+
+
 def max_over_ranks(value: float, device) -> float:
     """The largest `value` over all ranks (the step time that bounds the job)."""
     import torch
@@ -72,7 +101,7 @@ def max_over_ranks(value: float, device) -> float:
 
 
 def whole_job_tflops(flops_per_rank_step: float, world: int, max_ms: float) -> float:
-    """Work of all replicas divided by the slowest rank's step time."""
+    """Work of all shards divided by the slowest rank's step time."""
     return world * flops_per_rank_step / (max_ms * 1e-3) / 1e12
 
 
@@ -141,36 +170,60 @@ class ClockSampler:
 # the CPU oracle, timed on a bounded sample (reference arm and cpu_baseline)
 # --------------------------------------------------------------------------
 
-def oracle_step_seconds(wl, sample_tokens=256, sample_rows=64, head=0):
-    """Seconds the fp64 oracle needs for one whole step, extrapolated from one
-    head: calibrate (whole), append of `sample_tokens` keys, attention of
-    `sample_rows` query rows over the full cache.  Heads, tokens and rows are
-    independent, so the work scales linearly in each."""
+SAMPLE_TOKENS, SAMPLE_ROWS, SAMPLE_SEGMENTS = 512, 128, 16
+
+
+def oracle_sample(wl, head=0):
+    """Untimed set-up of the oracle's bounded sample of one step of `wl` for
+    one head: centroids, the historical queries, the last chunk's keys and
+    values, the query rows, and up to SAMPLE_SEGMENTS encoded segments of the
+    cache the attention reads."""
     from oracle import qwm_oracle as O
-    H, d, r, C = wl.heads, wl.head_dim, wl.rank, wl.n_centroids
+    C = wl.n_centroids
     kf = synth.kmeans_keys(wl, [head])[0]
     cent = synth.round_to_dtype(kf[synth.kmeans_init_rows(wl, head, kf.shape[1], C)], wl.dtype)
-    qh = synth.hist_queries(wl, 0, [head])[0]
-    t0 = time.perf_counter()
+    last = wl.n_chunks - 1
+    qh = synth.hist_queries(wl, last if wl.steps else 0, [head])[0]
     s = O.sensitivity(qh).astype(np.float32)
-    U, _, _ = O.psac_basis(qh, r)
+    U, _, _ = O.psac_basis(qh, wl.rank)
     w = O.group_weights(s)
-    t_cal = time.perf_counter() - t0
-    # cache of the 6-chunk prefix (untimed set-up)
+    n_seg = min(SAMPLE_SEGMENTS, wl.n_chunks)
     segs = [O.append_head(synth.keys(wl, ch, [head])[0], synth.values(wl, ch, [head])[0], cent, w, U)
-            for ch in range(wl.n_chunks - 1)]
-    k = synth.keys(wl, wl.n_chunks - 1, [head])[0]
-    v = synth.values(wl, wl.n_chunks - 1, [head])[0]
+            for ch in range(wl.n_chunks - n_seg, wl.n_chunks)]
+    return {"qh": qh, "cent": cent, "w": w, "U": U, "segs": segs, "n_seg": n_seg,
+            "k": synth.keys(wl, last, [head], n=SAMPLE_TOKENS)[0],
+            "v": synth.values(wl, last, [head], n=SAMPLE_TOKENS)[0],
+            "q": synth.queries(wl, last if wl.steps else 0, [head], m=SAMPLE_ROWS)[0]}
+
+
+def oracle_step(wl, smp):
+    """Time the oracle on the sample: calibrate (whole), append of
+    SAMPLE_TOKENS keys, attention of SAMPLE_ROWS rows over the sampled
+    segments.  Returns (seconds actually spent, extrapolated seconds of the
+    whole step of all heads, breakdown).  Heads, appended tokens, query rows
+    and cached segments are independent, so the work scales linearly."""
+    from oracle import qwm_oracle as O
     t0 = time.perf_counter()
-    O.append_head(k[:sample_tokens], v[:sample_tokens], cent, w, U)
-    t_app = (time.perf_counter() - t0) * wl.chunk / sample_tokens
-    segs.append(O.append_head(k, v, cent, w, U))
-    q = synth.queries(wl, 0, [head], m=sample_rows)[0]
-    t0 = time.perf_counter()
-    O.attend_head(q, segs, {0: U}, 1.0 / np.sqrt(d))
-    t_att = (time.perf_counter() - t0) * wl.n_query / sample_rows
-    per_head = t_cal + t_app + t_att
-    return per_head * H, {"calibrate_s": t_cal * H, "append_s": t_app * H, "attend_s": t_att * H}
+    s = O.sensitivity(smp["qh"]).astype(np.float32)
+    U, _, _ = O.psac_basis(smp["qh"], wl.rank)
+    w = O.group_weights(s)
+    t1 = time.perf_counter()
+    O.append_head(smp["k"], smp["v"], smp["cent"], w, U)
+    t2 = time.perf_counter()
+    O.attend_head(smp["q"], smp["segs"], {0: U}, 1.0 / np.sqrt(wl.head_dim))
+    t3 = time.perf_counter()
+    H = wl.heads
+    cal = (t1 - t0) * H
+    app = (t2 - t1) * H * wl.chunk / smp["k"].shape[0]
+    att = (t3 - t2) * H * (wl.n_query / smp["q"].shape[0]) * (wl.n_chunks / smp["n_seg"])
+    return t3 - t0, cal + app + att, {"calibrate_s": cal, "append_s": app, "attend_s": att}
+
+
+def oracle_sample_text(wl, smp):
+    return (f"1 of {wl.heads} heads: calibrate on {smp['qh'].shape[0]} queries (whole), append of "
+            f"{smp['k'].shape[0]} of {wl.chunk} tokens, attention of {smp['q'].shape[0]} of {wl.n_query} "
+            f"query rows over {smp['n_seg']} of {wl.n_chunks} cached segments; scaled linearly to the "
+            f"whole step (extrapolated)")
 
 
 def cpu_threads():
@@ -182,32 +235,45 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
+def one_thread_step_seconds(wl, smp):
+    """The same oracle step with its BLAS limited to one thread, or None."""
+    try:
+        from threadpoolctl import threadpool_limits
+    except Exception:
+        return None
+    with threadpool_limits(limits=1):
+        return oracle_step(wl, smp)[1]
+
+
 def run_reference(args):
     wl = synth.workload(args.workload)
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    smp = oracle_sample(wl)
     for _ in range(args.warmup):
-        oracle_step_seconds(wl, sample_tokens=64, sample_rows=16)
-    times = []
+        oracle_step(wl, smp)
+    spent, extrap = [], []
     for _ in range(args.steps):
-        sec, parts = oracle_step_seconds(wl)
-        times.append(sec)
-    step = float(np.mean(times))
+        sec, full, parts = oracle_step(wl, smp)
+        spent.append(sec)
+        extrap.append(full)
+    step = float(np.mean(extrap))
     N = wl.n_tokens
     value = attend_flops(wl.heads, wl.n_query, N, wl.head_dim, wl.rank) / step / 1e12
-    sample = (f"1 of {wl.heads} heads: calibrate whole, append 256 of {wl.chunk} tokens, attention "
-              f"of 64 of {wl.n_query} query rows over {N} tokens; scaled linearly (extrapolated)")
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": step * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "warmup": args.warmup, "ms_per_step": float(np.mean(spent)) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "heads": wl.heads, "head_dim": wl.head_dim,
                        "cached_tokens": N, "query_rows": wl.n_query, "chunk": wl.chunk,
                        "n_centroids": wl.n_centroids, "rank": wl.rank},
             "impl": "reference",
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": oracle_sample_text(wl, smp)},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "extrapolated_ms_per_step": step * 1e3,
+            "note": "ms_per_step is the time of the sampled step actually run; value is the whole "
+                    "step's work over the extrapolated whole-step time",
             "breakdown_s": parts}
     print(json.dumps(line), flush=True)
 
@@ -216,13 +282,12 @@ def run_reference(args):
 # the GPU arm
 # --------------------------------------------------------------------------
 
-def run_gpu(args):
+def _gpu_init(args):
     import torch
     import torch.distributed as dist
     from bit_kv_cache_qwm_gb300 import build as B
     B.build()
     from bit_kv_cache_qwm_gb300 import qwm
-
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -230,31 +295,63 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
+    return torch, dist, qwm, world, rank, local, dev
 
-    wl = synth.workload(args.workload)
-    H, d, r, C = wl.heads, wl.head_dim, wl.rank, wl.n_centroids
+
+def _generate(fn, items, threads=16):
+    """Draw synthetic arrays in parallel threads (numpy's generators release
+    the GIL while filling); the results are in `items` order."""
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(fn, items))
+
+
+def build_stream(torch, qwm, wl, heads, dev, kernel):
+    """Context for `heads` of workload `wl` holding the cache of its first
+    n_chunks - 1 steps.  Streaming workloads recalibrate before every append
+    (one basis version per segment); the others calibrate once.  Returns
+    (ctx, inputs of the last step as device tensors)."""
+    H, d, r, C = len(heads), wl.head_dim, wl.rank, wl.n_centroids
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     n_prefix = wl.n_chunks - 1
 
     def T(x):
         return torch.from_numpy(np.ascontiguousarray(x)).to(dev, tdt)
 
-    # inputs: every rank holds its own replica of the workload (weak scaling)
-    kf = synth.kmeans_keys(wl)
-    rows = np.stack([synth.kmeans_init_rows(wl, h, kf.shape[1], C) for h in range(H)]).astype(np.int32)
+    kf = synth.kmeans_keys(wl, heads)
+    rows = np.stack([synth.kmeans_init_rows(wl, h, kf.shape[1], C) for h in heads]).astype(np.int32)
     tiles = wl.n_chunks * ((wl.chunk + 127) // 128)
-    ctx = qwm.Qwm(H, d, r, C, dtype=wl.dtype, max_tokens=tiles * 128, max_versions=2,
-                  max_hist=wl.n_hist, device=dev)
+    ctx = qwm.Qwm(H, d, r, C, dtype=wl.dtype, max_tokens=tiles * 128,
+                  max_versions=(wl.n_chunks + 1) if wl.steps else 2, max_hist=wl.n_hist, device=dev)
     # the centroids: 25 Lloyd iterations on the keys of frame 0, on the GPU
-    cent = qwm.qwm_kmeans(T(kf), torch.from_numpy(rows).to(dev), C, iters=25)
-    ctx.set_centroids(cent)
-    ctx.set_attend_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4}[args.kernel])
-    qh = T(synth.hist_queries(wl, 0))
-    ctx.calibrate(qh)
-    for ch in range(n_prefix):
-        ctx.append(T(synth.keys(wl, ch)), T(synth.values(wl, ch)))
-    k_new, v_new = T(synth.keys(wl, n_prefix)), T(synth.values(wl, n_prefix))
-    q = T(synth.queries(wl, 0))
+    ctx.set_centroids(qwm.qwm_kmeans(T(kf), torch.from_numpy(rows).to(dev), C, iters=25))
+    ctx.set_attend_kernel(KERNEL_IDS[kernel])
+
+    def draw(ch):
+        qh = synth.hist_queries(wl, ch, heads) if (wl.steps or ch == 0) else None
+        return qh, synth.keys(wl, ch, heads), synth.values(wl, ch, heads)
+
+    # drawn 16 steps at a time (bounded host memory), appended in order
+    for b0 in range(0, n_prefix, 16):
+        for ch, (qh, k, v) in zip(range(b0, n_prefix), _generate(draw, range(b0, min(b0 + 16, n_prefix)))):
+            if qh is not None:
+                ctx.calibrate(T(qh))
+            ctx.append(T(k), T(v))
+    last = n_prefix
+    qh, k, v = draw(last)
+    if qh is None:
+        qh = synth.hist_queries(wl, 0, heads)
+    inp = {"qh": T(qh), "k": T(k), "v": T(v), "q": T(synth.queries(wl, last if wl.steps else 0, heads))}
+    return ctx, inp
+
+
+def run_gpu(args):
+    torch, dist, qwm, world, rank, local, dev = _gpu_init(args)
+    wl = synth.workload(args.workload)
+    heads = shard_heads(rank, world, wl.heads)
+    H, d, r, C = wl.heads, wl.head_dim, wl.rank, wl.n_centroids
+    n_prefix = wl.n_chunks - 1
+    ctx, inp = build_stream(torch, qwm, wl, heads, dev, args.kernel)
+    qh, k_new, v_new, q = inp["qh"], inp["k"], inp["v"], inp["q"]
     out = torch.empty_like(q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -262,19 +359,22 @@ def run_gpu(args):
 
     N = wl.n_tokens
     if args.only:
-        # profiling mode: the cache holds the full workload, then only the named
-        # call runs, --steps times (no timing, no JSON line)
+        # profiling mode: the cache holds the prefix; only the named call runs,
+        # --steps times (no timing, no JSON line)
         if args.only == "attend":
+            ctx.calibrate(qh)
             ctx.append(k_new, v_new)
             for _ in range(args.steps):
                 ctx.attend(q, out)
         elif args.only == "append":
+            ctx.calibrate(qh)
             for _ in range(args.steps):
                 ctx.append(k_new, v_new)
                 ctx.rewind(n_prefix)
         else:
             for _ in range(args.steps):
                 ctx.calibrate(qh)
+                ctx.rewind(n_prefix)
         torch.cuda.synchronize()
         assert ctx.status() == 0
         return
@@ -320,6 +420,25 @@ def run_gpu(args):
     att = [e[2].elapsed_time(e[3]) for e in evs]
     stp = [e[0].elapsed_time(e[3]) for e in evs]
     ms_step = max_over_ranks(float(np.mean(stp)), dev)
+    out_ref = out.clone()
+
+    # the append kernels alone (quantisation and PSAC coefficients), with the
+    # step's calibration already in place: the HBM roofline of the append
+    ctx.calibrate(qh)
+    torch.cuda.synchronize()
+    app_alone = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ctx.append(k_new, v_new)
+        e1.record(stream)
+        ctx.rewind(n_prefix)
+        if i >= args.warmup:
+            app_alone.append((e0, e1))
+    torch.cuda.synchronize()
+    app_ms = float(np.mean([a.elapsed_time(b) for a, b in app_alone]))
+    ctx.rewind(n_prefix)
 
     # end to end through the public API with host buffers (pinned): every
     # step's inputs go host -> device and its output comes back, all inside
@@ -377,41 +496,55 @@ def run_gpu(args):
         pipelined(args.warmup)
     e2e_step = max_over_ranks(pipelined(args.steps), dev)
     # the last end-to-end output is the device-timed steps' output (same inputs)
-    e2e_same = bool(torch.equal(h_out[(args.steps - 1) & 1], out.cpu()))
+    e2e_same = bool(torch.equal(h_out[(args.steps - 1) & 1], out_ref.cpu()))
     h2d = sum(x.numel() * x.element_size() for x in h_in)
     d2h = h_out[0].numel() * h_out[0].element_size()
+    st = st | ctx.status()
 
     peaks = load_peaks()
     att_ms = float(np.mean(att))
     achieved = flops / (att_ms * 1e-3) / 1e12
     value = whole_job_tflops(flops, world, ms_step)
-    kernel = {0: "auto", 1: "simt", 2: "mma", 3: "tcgen05", 4: "tcgen05-2tile"}
+    kern = ctx.resolved_attend_kernel
+    in_elem = 2 if wl.dtype == "bf16" else 4
+    app_bytes = H * wl.chunk * append_bytes_per_token_head(d, ctx.layout.bytes_per_token, in_elem)
+    app_gbs = app_bytes / (app_ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "heads": H, "head_dim": d, "cached_tokens": N,
                    "query_rows": wl.n_query, "chunk": wl.chunk, "n_centroids": C, "rank": r,
-                   "hist_queries": wl.n_hist, "parallelism": f"replicas x{world}",
+                   "hist_queries": wl.n_hist, "basis_versions_in_cache": wl.n_chunks if wl.steps else 1,
+                   "parallelism": f"head shards x{world} (heads {heads[0]}-{heads[-1]} on rank {rank})",
                    "l2": "flushed between steps (256 MiB write)",
                    "centroids": "k-means on frame 0 (25 Lloyd iterations, GPU)"},
         "components": {"calibrate_ms": float(np.mean(cal)), "append_ms": float(np.mean(app)),
                        "attend_ms": att_ms, "attend_tflops": achieved,
                        "cache_gbs": cache_bytes / (att_ms * 1e-3) / 1e9,
-                       "append_mtok_s": wl.chunk / (float(np.mean(app)) * 1e-3) / 1e6,
-                       "append_gbs": H * wl.chunk * (4 * d + ctx.layout.bytes_per_token) / (float(np.mean(app)) * 1e-3) / 1e9,
-                       "attend_kernel": kernel.get(ctx.resolved_attend_kernel, "?")},
+                       "append_alone_ms": app_ms,
+                       "append_mtok_s": wl.chunk / (app_ms * 1e-3) / 1e6,
+                       "append_token_heads_per_s": H * wl.chunk / (app_ms * 1e-3),
+                       "attend_kernel": KERNEL_NAMES.get(kern, "?")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],
                      "traffic": profiled_traffic(os.path.join(ROOT, "profiles", f"attend_tc2_{wl.name}.md"),
                                                  os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc", "attend_tc.cu"))
-                     if ctx.resolved_attend_kernel == 4 else None,
-                     "kernel": "qwm_attend", "peak_source": peaks["source"] + " burst bf16"},
+                     if kern == 4 else None,
+                     "kernel": "qwm_attend", "peak_source": peaks["source"] + " burst bf16",
+                     "work": "H (4 M N d + 2 M N r + 2 M d r) flops per launch"},
+        "roofline_append": {"bound": "hbm", "achieved": app_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": app_gbs / peaks["hbm_gbs"], "kernel": "qwm_append",
+                            "bytes_per_token_head": append_bytes_per_token_head(d, ctx.layout.bytes_per_token,
+                                                                                in_elem),
+                            "traffic": profiled_traffic(os.path.join(ROOT, "profiles", f"append_{wl.name}.md"),
+                                                        os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc",
+                                                                     "append.cu")),
+                            "peak_source": peaks["source"] + " HBM copy"},
         "e2e": {"value": world * flops / (e2e_step * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step,
                 "copies": "second stream, double-buffered: inputs of step i+1 and output of step i-1 "
                           "move while step i computes", "output_matches_device_timed": e2e_same},
-        # gram, gram sum, A^2, eig, weights, append, attend (A^2 only when r > 0)
         # gram, gram_sum, [square], eig, weights, append, [append_e], attend
         "gpu_launches": args.steps * (8 if r > 0 else 6),
         "clocks": clk.summary(),
@@ -419,13 +552,83 @@ def run_gpu(args):
         "device_status": int(st),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sec, parts = oracle_step_seconds(wl)
+        smp = oracle_sample(wl)
+        oracle_step(wl, smp)                          # warm-up
+        runs = []
+        while sum(x[0] for x in runs) < 10.0:        # about 10 s of CPU work
+            runs.append(oracle_step(wl, smp))
+        spent = float(np.mean([x[0] for x in runs]))
+        full = float(np.mean([x[1] for x in runs]))
+        parts = {k: float(np.mean([x[2][k] for x in runs])) for k in runs[0][2]}
+        one = one_thread_step_seconds(wl, smp)
         line["cpu_baseline"] = {
-            "value": flops / sec / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
-            "sample": "1 head: calibrate whole, append 256 of 4680 tokens, attention of 64 of 4680 rows "
-                      "over 32760 tokens; scaled to 12 heads (extrapolated)", "step_s": sec}
+            "value": flops / full / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": oracle_sample_text(wl, smp) + f"; {len(runs)} repetitions averaged",
+            "step_s": full, "sample_s": spent, "breakdown_s": parts,
+            "value_1_thread": (flops / one / 1e12) if one else None}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_sweep(args):
+    """The append-only sweep: for every (chunk length, centroids, rank) point,
+    one JSON line with the append's Mtokens/s and its HBM fraction."""
+    torch, dist, qwm, world, rank, local, dev = _gpu_init(args)
+    wl = synth.workload("bf16-h24-append-sweep")
+    heads = shard_heads(rank, world, wl.heads)
+    H, d = wl.heads, wl.head_dim
+    T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev, torch.bfloat16)
+    n_max = max(wl.sweep["chunk"])
+    k_all, v_all = T(synth.keys(wl, 1, heads, n=n_max)), T(synth.values(wl, 1, heads, n=n_max))
+    qh = T(synth.hist_queries(wl, 0, heads))
+    kf = synth.kmeans_keys(wl, heads)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+    points = [(n, C, r) for C in wl.sweep["n_centroids"] for r in wl.sweep["rank"] for n in wl.sweep["chunk"]]
+    if args.sweep_points:
+        points = points[: args.sweep_points]
+    cents = {}
+    for n, C, r in points:
+        if C not in cents:
+            rows = np.stack([synth.kmeans_init_rows(wl, h, kf.shape[1], C) for h in heads]).astype(np.int32)
+            cents[C] = qwm.qwm_kmeans(T(kf), torch.from_numpy(rows).to(dev), C, iters=25)
+        ctx = qwm.Qwm(H, d, r, C, dtype="bf16", max_tokens=((n + 127) // 128) * 128, max_versions=2,
+                      max_hist=wl.n_hist, device=dev)
+        ctx.set_centroids(cents[C])
+        ctx.calibrate(qh)
+        k, v = k_all[:, :n].contiguous(), v_all[:, :n].contiguous()
+        evs = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ctx.append(k, v)
+            e1.record(stream)
+            ctx.rewind(0)
+            if i >= args.warmup:
+                evs.append((e0, e1))
+        torch.cuda.synchronize()
+        st = ctx.status()
+        ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in evs])), dev)
+        bpt = append_bytes_per_token_head(d, ctx.layout.bytes_per_token)
+        gbs = world * H * n * bpt / (ms * 1e-3) / 1e9
+        line = {"metric": "qwm_append Mtokens/s", "value": world * n / (ms * 1e-3) / 1e6, "unit": "Mtokens/s",
+                "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": wl.name, "heads": H, "head_dim": d, "chunk": n, "n_centroids": C,
+                           "rank": r, "l2": "flushed between steps (256 MiB write)"},
+                "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": gbs / peaks["hbm_gbs"], "bytes_per_token_head": bpt,
+                             "peak_source": peaks["source"] + " HBM copy"},
+                "token_heads_per_s": world * H * n / (ms * 1e-3),
+                "gpu_launches": args.steps * (2 if r > 0 else 1), "device_status": int(st)}
+        ctx.close()
+        if rank == 0:
+            print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
@@ -434,25 +637,15 @@ def run_small_m(args):
     """Few query rows (--small-m M) over the workload's whole cache: the
     attention is bound by reading the packed cache, so the metric is cache
     GB/s against the measured HBM copy bandwidth.  Prints its own JSON line."""
-    import torch
-    from bit_kv_cache_qwm_gb300 import build as B
-    B.build()
-    from bit_kv_cache_qwm_gb300 import qwm
+    torch, dist, qwm, world, rank, local, dev = _gpu_init(args)
     wl = synth.workload(args.workload)
+    heads = shard_heads(rank, world, wl.heads)
     H, d, r, C, M = wl.heads, wl.head_dim, wl.rank, wl.n_centroids, args.small_m
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    T = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev, torch.bfloat16)
-    kf = synth.kmeans_keys(wl)
-    rows = np.stack([synth.kmeans_init_rows(wl, h, kf.shape[1], C) for h in range(H)]).astype(np.int32)
-    tiles = wl.n_chunks * ((wl.chunk + 127) // 128)
-    ctx = qwm.Qwm(H, d, r, C, dtype=wl.dtype, max_tokens=tiles * 128, max_hist=wl.n_hist, device=dev)
-    ctx.set_centroids(qwm.qwm_kmeans(T(kf), torch.from_numpy(rows).to(dev), C, iters=25))
-    ctx.calibrate(T(synth.hist_queries(wl, 0)))
-    for ch in range(wl.n_chunks):
-        ctx.append(T(synth.keys(wl, ch)), T(synth.values(wl, ch)))
-    ctx.set_attend_kernel({"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4}[args.kernel])
-    q = T(synth.queries(wl, 0, m=M))
+    ctx, inp = build_stream(torch, qwm, wl, heads, dev, args.kernel)
+    ctx.calibrate(inp["qh"])
+    ctx.append(inp["k"], inp["v"])
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    q = torch.from_numpy(synth.queries(wl, wl.n_chunks - 1 if wl.steps else 0, heads, m=M)).to(dev, tdt)
     out = torch.empty_like(q)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
@@ -466,14 +659,16 @@ def run_small_m(args):
         ctx.attend(q, out)
     torch.cuda.synchronize()
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    with ClockSampler(0) as clk:
+    if world > 1:
+        dist.barrier()
+    with ClockSampler(local) as clk:
         for e0, e1 in evs:
             flush.zero_()
             e0.record(stream)
             ctx.attend(q, out)
             e1.record(stream)
         torch.cuda.synchronize()
-    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+    ms = max_over_ranks(float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs])), dev)
     st = ctx.status()
     # end to end: Q from pinned host memory, O back to it, inside the timed region
     h_q = q.cpu().pin_memory()
@@ -491,11 +686,11 @@ def run_small_m(args):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e.append(e0.elapsed_time(e1))
-    e2e_ms = float(np.mean(e2e))
+    e2e_ms = max_over_ranks(float(np.mean(e2e)), dev)
     peaks = load_peaks()
     gbs = nbytes / (ms * 1e-3) / 1e9
     line = {
-        "metric": f"qwm_attend cache GB/s, {M} query rows", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "metric": f"qwm_attend cache GB/s, {M} query rows", "value": world * gbs, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": {"workload": wl.name, "heads": H, "head_dim": d, "cached_tokens": N, "query_rows": M,
@@ -508,7 +703,7 @@ def run_small_m(args):
                      if kern == 5 else None,
                      "kernel": "qwm_attend",
                      "bytes_per_launch": nbytes, "peak_source": peaks["source"] + " HBM copy"},
-        "e2e": {"value": nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": q.numel() * q.element_size(),
                 "d2h_bytes_per_step": out.numel() * out.element_size(), "ms_per_step": e2e_ms},
         "gpu_launches": args.steps * (3 if kern == 5 else 1),
@@ -516,7 +711,10 @@ def run_small_m(args):
         "device_status": int(st),
         "attend_tflops": attend_flops(H, M, N, d, r) / (ms * 1e-3) / 1e12,
     }
-    print(json.dumps(line), flush=True)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
 
 
 def main():
@@ -525,19 +723,23 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="qwm", choices=["qwm", "reference"])
-    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", choices=["", "attend", "append", "calibrate"],
                     help="profiling mode: set up the workload, then run only this call --steps times")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma", "tc", "tc2"],
+    ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_IDS),
                     help="attention kernel (auto picks the fastest that applies)")
     ap.add_argument("--small-m", type=int, default=0,
                     help="few-row attention: M query rows over the workload's whole cache (GB/s line)")
+    ap.add_argument("--sweep", action="store_true", help="the append-only sweep, one JSON line per point")
+    ap.add_argument("--sweep-points", type=int, default=0, help="only the first N sweep points")
     args = ap.parse_args()
-    if args.small_m > 0 and args.impl != "reference":
-        run_small_m(args)
-    elif args.impl == "reference":
+    if args.impl == "reference":
         run_reference(args)
+    elif args.sweep:
+        run_sweep(args)
+    elif args.small_m > 0:
+        run_small_m(args)
     else:
         run_gpu(args)
 

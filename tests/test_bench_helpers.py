@@ -3,6 +3,7 @@ a committed ncu summary only while that summary's recorded source hash matches
 the kernel source; the whole-job value scales with the number of replicas."""
 import hashlib
 import os
+import re
 import sys
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -27,16 +28,31 @@ def test_traffic_only_for_the_captured_source(tmp_path):
 
 
 def test_committed_summaries_name_their_sources():
-    """Every committed kernel summary that bench.py reads records a source hash
-    and a per-launch DRAM byte count in the machine-readable form."""
+    """Every committed kernel summary that records a source hash also records
+    a per-launch DRAM byte count in the machine-readable form, and names a
+    source file that exists."""
     prof = os.path.join(ROOT, "profiles")
-    for name, src in (("attend_tc2_bf16-h12-n32760.md", "attend_tc.cu"),
-                      ("attend_small_bf16-h40-n98280-outlier_m16.md", "attend_small.cu")):
-        path = os.path.join(prof, name)
-        text = open(path).read()
-        assert "source sha256: " in text and "dram bytes per launch: " in text, name
-        got = bench.profiled_traffic(path, os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc", src))
+    csrc = os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc")
+    for name in sorted(os.listdir(prof)):
+        text = open(os.path.join(prof, name)).read()
+        if "source sha256: " not in text:
+            continue
+        assert "dram bytes per launch: " in text, name
+        src = re.search(r"bit_kv_cache_qwm_gb300/csrc/([a-z_0-9]+\.cu)", text)
+        assert src and os.path.exists(os.path.join(csrc, src.group(1))), name
+        got = bench.profiled_traffic(os.path.join(prof, name), os.path.join(csrc, src.group(1)))
         assert got is None or got > 0
+
+
+def test_append_bytes_and_oracle_extrapolation():
+    """641 B per token-head at d = 128 (bf16 k and v in, 129 B out), and the
+    oracle sample's extrapolation scales each part by what it left out."""
+    assert bench.append_bytes_per_token_head(128, 129) == 641
+    wl = bench.synth.workload("tiny-f32-h1-n1024")
+    smp = bench.oracle_sample(wl)
+    spent, full, parts = bench.oracle_step(wl, smp)
+    assert spent > 0 and full >= spent * 0.5
+    assert abs(sum(parts.values()) - full) < 1e-9 * max(full, 1.0)
 
 
 def test_whole_job_value_scales_with_replicas():
