@@ -235,14 +235,20 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
-def one_thread_step_seconds(wl, smp):
-    """The same oracle step with its BLAS limited to one thread, or None."""
+def one_thread_step_seconds(wl):
+    """Extrapolated seconds of the same oracle step with every BLAS and OpenMP
+    pool limited to one thread, timed in a child process (the thread counts of
+    numpy's BLAS are fixed when it loads), or None if that fails."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    code = ("import sys; sys.path.insert(0, %r); import bench; from bit_kv_cache_qwm_gb300 import synth; "
+            "wl = synth.workload(%r); smp = bench.oracle_sample(wl); bench.oracle_step(wl, smp); "
+            "print(bench.oracle_step(wl, smp)[1])" % (ROOT, wl.name))
     try:
-        from threadpoolctl import threadpool_limits
-    except Exception:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        return float(out.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError, OSError):
         return None
-    with threadpool_limits(limits=1):
-        return oracle_step(wl, smp)[1]
 
 
 def run_reference(args):
@@ -560,7 +566,7 @@ def run_gpu(args):
         spent = float(np.mean([x[0] for x in runs]))
         full = float(np.mean([x[1] for x in runs]))
         parts = {k: float(np.mean([x[2][k] for x in runs])) for k in runs[0][2]}
-        one = one_thread_step_seconds(wl, smp)
+        one = one_thread_step_seconds(wl)
         line["cpu_baseline"] = {
             "value": flops / full / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
             "sample": oracle_sample_text(wl, smp) + f"; {len(runs)} repetitions averaged",

@@ -5,23 +5,30 @@
 // projections".  roboind article, "Step 2": the energy of historical queries
 // concentrates in a few directions.
 //
-// 1. gram_kernel: partial Gram matrices Q^T Q of row blocks (float32 FMA,
-//    fixed order), one CTA per (head, row block).
-// 2. eig_kernel, one CTA per head: sums the partials in a fixed order, writes
-//    s_c = G_cc / n_h, then finds the top-r eigenvectors of G by block
-//    subspace iteration on G^2 (start block = unit vectors of the largest
-//    diagonal entries, modified Gram-Schmidt twice per step) with a two-pass
-//    Rayleigh-Ritz (parallel cyclic Jacobi on the projected matrix, then once
-//    more on the re-orthonormalised Ritz vectors, which restores
-//    orthogonality to float32 precision).  When r + oversample exceeds 64 the
-//    whole matrix goes through Jacobi instead.  Every loop has a fixed bound;
-//    a miss of the residual tolerance sets QWM_DEV_NOT_CONVERGED.
-// 3. weights_kernel: w_g = s_{32g} + ... + s_{32g+31}, left to right in
+// 1. gram_kernel: partial Gram matrices Q^T Q of 128-row blocks (float32
+//    FMA, fixed order), one CTA per (head, row block).
+// 2. gram_sum_kernel: adds the partials in split order (many CTAs) and writes
+//    s_c = G_cc / n_h.
+// 3. square_kernel: A^2 = (G scale + 2^-20 I)^2 tile by tile (the scale makes
+//    the mean eigenvalue 1).
+// 4. eig_kernel, one CTA per head: the top-r eigenvectors of G by block
+//    subspace iteration on A^2 (start block = unit vectors of the largest
+//    diagonal entries; modified Gram-Schmidt once per step, twice before a
+//    convergence check), a Rayleigh-Ritz check after kFirstCheck steps and
+//    then every kCheckEvery (parallel cyclic Jacobi on the projected matrix),
+//    and on the converged Ritz vectors one more Gram-Schmidt pass and
+//    Rayleigh-Ritz pass, which restores orthogonality to float32 precision.
+//    When r + oversample exceeds 64 the whole matrix goes through Jacobi
+//    instead.  Every loop has a fixed bound; a miss of the residual tolerance
+//    sets QWM_DEV_NOT_CONVERGED.
+// 5. weights_kernel: w_g = s_{32g} + ... + s_{32g+31}, left to right in
 //    float32 (an input of the centroid decision).
 #include <math.h>
 #include <string.h>
 
 #include <mutex>
+
+#include <cuda.h>
 
 #include "qwm_internal.cuh"
 
@@ -1024,24 +1031,61 @@ constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) float g_calib_scratch[kStaticScratchBytes / sizeof(float)];
 
 constexpr int kMaxDevices = 64;
-static float* g_scratch_ptr[kMaxDevices];
+struct ScratchAddr {
+  unsigned long long ctx_id;   // driver context the address belongs to
+  float* ptr;
+};
+static ScratchAddr g_scratch_addr[kMaxDevices];
 static std::mutex g_scratch_mu;
 
-// Device address of the scratch array on the current device, looked up once
-// per device (host code cannot use the symbol itself as a device address).
+// The driver's id of the current context (unique for the life of the
+// process, unlike the context handle, which a new context may reuse), or 0
+// when none is current.  Found through the runtime's driver entry points, so
+// the library does not link the driver library itself.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+unsigned long long current_ctx_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    cudaDriverEntryPointQueryResult q1, q2;
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) == cudaSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) == cudaSuccess &&
+        q1 == cudaDriverEntryPointSuccess && q2 == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+      get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    }
+    looked_up = true;
+  }
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch array in the current context.  It is looked
+// up once per device and context (host code cannot use the symbol itself as a
+// device address); a new context on the device (after cudaDeviceReset, for
+// instance) has a new id, so its first call looks the address up again.
 cudaError_t static_scratch(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  const unsigned long long id = current_ctx_id();
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (!a.ptr || id == 0 || a.ctx_id != id) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_calib_scratch);
+    e = cudaGetSymbolAddress(&p, g_calib_scratch);   // makes the primary context current if none was
     if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
+    a.ptr = static_cast<float*>(p);
+    a.ctx_id = current_ctx_id();
   }
-  *out = g_scratch_ptr[dev];
+  *out = a.ptr;
   return cudaSuccess;
 }
 

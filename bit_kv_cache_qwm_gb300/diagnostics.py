@@ -23,6 +23,10 @@ encoding:
   output_rel_error             both quantised (what qwm_attend computes)
 
   python -m bit_kv_cache_qwm_gb300.diagnostics --workload bf16-h12-n32760 --heads 0,1,2,3 --rows 256
+
+This module is a measurement tool, not part of the product path: its
+comparisons run in eager torch on dequantised copies, and no library call
+(calibrate, append, attend) uses it.
 """
 import argparse
 import json

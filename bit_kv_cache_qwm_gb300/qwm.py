@@ -19,7 +19,10 @@ LIB_PATH = os.path.join(_PKG, "libqwm.so")
 
 QWM_F32, QWM_BF16 = 0, 1
 DEV_NOT_CONVERGED, DEV_SATURATED = 0x1, 0x2
-KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA, KERNEL_TC = 0, 1, 2, 3
+# attention kernels (qwm_set_attend_kernel): automatic choice, float32 SIMT,
+# bf16 mma.sync, tcgen05 with one query tile per CTA, tcgen05 with two query
+# tiles per CTA, few-row split-KV (M <= 64)
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA, KERNEL_TC, KERNEL_TC2, KERNEL_SMALL = 0, 1, 2, 3, 4, 5
 
 STATUS = {0: "QWM_OK", 1: "QWM_ERR_INVALID_ARG", 2: "QWM_ERR_UNSUPPORTED", 3: "QWM_ERR_CAPACITY",
           4: "QWM_ERR_NOT_CALIBRATED", 5: "QWM_ERR_NOT_CONVERGED", 6: "QWM_ERR_CUDA",
@@ -122,46 +125,75 @@ def _fptr(a: Optional[np.ndarray]):
     return a.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
 
 
+def _device_tensor(x, what: str, dtypes, ndim: int) -> torch.Tensor:
+    """A contiguous CUDA tensor of one of `dtypes` with `ndim` dimensions, or ValueError."""
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError(f"{what}: a CUDA tensor is expected")
+    if x.dtype not in dtypes or x.dim() != ndim or not x.is_contiguous():
+        raise ValueError(f"{what}: a contiguous {ndim}-d tensor of {dtypes} is expected, got "
+                         f"{x.dtype} {tuple(x.shape)}")
+    return x
+
+
+def _out_tensor(t, what: str, dtype, shape, device) -> torch.Tensor:
+    if (not isinstance(t, torch.Tensor) or t.device != device or t.dtype != dtype
+            or tuple(t.shape) != tuple(shape) or not t.is_contiguous()):
+        raise ValueError(f"out[{what!r}]: a contiguous {dtype} tensor of shape {tuple(shape)} on {device} "
+                         f"is expected")
+    return t
+
+
 def qwm_calibrate_static(q_hist: torch.Tensor, rank: int, max_iter: int = 64, oversample: int = 16,
                          out: Optional[dict] = None) -> dict:
     """Calibration that allocates nothing on the device inside the library
     (scratch in a fixed 8 MiB array of the library).  Output buffers are taken
-    from `out` when given (torch float32 tensors on q_hist's device), else
-    allocated here by torch, outside the library."""
+    from `out` when given (contiguous float32 tensors on q_hist's device, and
+    an int32 status word of one element), else allocated here by torch,
+    outside the library.  Runs on q_hist's device and that device's current
+    stream."""
+    q_hist = _device_tensor(q_hist, "q_hist", (torch.bfloat16, torch.float32), 3)
     H, n_h, d = q_hist.shape
     dt = QWM_BF16 if q_hist.dtype == torch.bfloat16 else QWM_F32
-    if not q_hist.is_contiguous() or q_hist.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("q_hist: contiguous bf16 or f32 tensor expected")
     dev = q_hist.device
+    rr = max(rank, 1)
+    shapes = {"s": ((H, d), torch.float32), "U": ((H, rr, d), torch.float32),
+              "lambda": ((H, rr), torch.float32), "energy": ((H,), torch.float32),
+              "status": ((1,), torch.int32)}
     if out is None:
-        out = {"s": torch.empty(H, d, dtype=torch.float32, device=dev),
-               "U": torch.empty(H, max(rank, 1), d, dtype=torch.float32, device=dev),
-               "lambda": torch.empty(H, max(rank, 1), dtype=torch.float32, device=dev),
-               "energy": torch.empty(H, dtype=torch.float32, device=dev),
-               "status": torch.zeros(1, dtype=torch.int32, device=dev)}
+        out = {k: torch.empty(sh, dtype=dt_, device=dev) for k, (sh, dt_) in shapes.items()}
+        out["status"].zero_()
+    else:
+        for k, (sh, dt_) in shapes.items():
+            _out_tensor(out.get(k), k, dt_, sh, dev)
     P = lambda t: ctypes.c_void_p(t.data_ptr())
-    _check(lib().qwm_calibrate_static(H, d, rank, dt, max_iter, oversample, P(q_hist), n_h, P(out["s"]),
-                                      P(out["U"]), P(out["lambda"]), P(out["energy"]), P(out["status"]),
-                                      _stream()), "qwm_calibrate_static")
+    with torch.cuda.device(dev):
+        _check(lib().qwm_calibrate_static(H, d, rank, dt, max_iter, oversample, P(q_hist), n_h, P(out["s"]),
+                                          P(out["U"]), P(out["lambda"]), P(out["energy"]), P(out["status"]),
+                                          _stream()), "qwm_calibrate_static")
     return out
 
 
 def qwm_kmeans(keys: torch.Tensor, init_rows: torch.Tensor, n_centroids: int, iters: int = 25) -> torch.Tensor:
-    """Lloyd's k-means on the GPU: keys [H][n][d] (bf16/f32), init_rows [H][C]
-    int32 on the same device.  Returns centroids [H][C][d] in the keys' dtype."""
+    """Lloyd's k-means on the GPU: keys [H][n][d] (bf16/f32, CUDA), init_rows
+    [H][C] integer row indices (moved to the keys' device).  Returns centroids
+    [H][C][d] in the keys' dtype, on the keys' device."""
+    keys = _device_tensor(keys, "keys", (torch.bfloat16, torch.float32), 3)
     H, n, d = keys.shape
     dt = QWM_BF16 if keys.dtype == torch.bfloat16 else QWM_F32
-    if not keys.is_contiguous() or keys.dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("keys: contiguous bf16 or f32 tensor expected")
-    rows = init_rows.to(device=keys.device, dtype=torch.int32).contiguous()
-    if tuple(rows.shape) != (H, n_centroids):
+    if not isinstance(init_rows, torch.Tensor) or init_rows.dtype.is_floating_point:
+        raise ValueError("init_rows: an integer tensor is expected")
+    if tuple(init_rows.shape) != (H, n_centroids):
         raise ValueError("init_rows: shape [H, C] expected")
-    ws = torch.empty(lib().qwm_kmeans_workspace_bytes(H, d, n_centroids, n) + 256, dtype=torch.uint8,
-                     device=keys.device)
-    out = torch.empty((H, n_centroids, d), dtype=keys.dtype, device=keys.device)
-    _check(lib().qwm_kmeans(H, d, dt, n_centroids, ctypes.c_void_p(keys.data_ptr()), n,
-                            ctypes.c_void_p(rows.data_ptr()), iters, ctypes.c_void_p(out.data_ptr()),
-                            ctypes.c_void_p(ws.data_ptr()), _stream()), "qwm_kmeans")
+    if not 1 <= n_centroids <= n:
+        raise ValueError("n_centroids: between 1 and the number of keys")
+    rows = init_rows.to(device=keys.device, dtype=torch.int32).contiguous()
+    with torch.cuda.device(keys.device):
+        ws = torch.empty(lib().qwm_kmeans_workspace_bytes(H, d, n_centroids, n) + 256, dtype=torch.uint8,
+                         device=keys.device)
+        out = torch.empty((H, n_centroids, d), dtype=keys.dtype, device=keys.device)
+        _check(lib().qwm_kmeans(H, d, dt, n_centroids, ctypes.c_void_p(keys.data_ptr()), n,
+                                ctypes.c_void_p(rows.data_ptr()), iters, ctypes.c_void_p(out.data_ptr()),
+                                ctypes.c_void_p(ws.data_ptr()), _stream()), "qwm_kmeans")
     return out
 
 

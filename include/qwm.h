@@ -168,14 +168,19 @@ qwm_status qwm_calibrate(qwm_ctx* ctx, const void* d_q_hist, int64_t n_h, void* 
  *     requests return QWM_ERR_CAPACITY before any launch.  That is up to 63
  *     heads at d = 128 (18 when rank + oversample > 64) and 255 at d = 64.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) once for that device; make that first call before
- *     any stream capture.  No call allocates or frees memory.
+ *     (cudaGetSymbolAddress) once for that device and its current context;
+ *     make that first call before any stream capture.  A new context on the
+ *     device (after cudaDeviceReset, for instance) has a new driver id, and
+ *     the first call in it looks the address up again (also before any
+ *     capture).  No call allocates or frees memory.
  *   - All calls share the one array: calls that overlap on the GPU (two
  *     streams, or two host threads) race and corrupt each other's results;
  *     order them.  Nothing in the array needs to start at zero except the
  *     status word, which the call clears itself.
  *   - d_status (optional, caller-zeroed) receives QWM_DEV_NOT_CONVERGED when
- *     the eigen-solver hits max_iter.  Asynchronous on `stream`. */
+ *     the eigen-solver hits max_iter.  With d_status NULL that bit goes to a
+ *     word of the shared array and is not reported: a caller that needs to
+ *     know about non-convergence passes d_status.  Asynchronous on `stream`. */
 qwm_status qwm_calibrate_static(int32_t heads, int32_t head_dim, int32_t rank, int32_t dtype,
                                 int32_t max_iter, int32_t oversample, const void* d_q_hist,
                                 int64_t n_h, float* d_s, float* d_U, float* d_lambda,

@@ -85,3 +85,19 @@ def test_null_context_calls_fail_cleanly(qwm):
     assert L.qwm_destroy(None) == 0
     for s in range(9):
         assert L.qwm_status_string(s)
+
+
+def test_static_calibration_and_kmeans_reject_host_tensors():
+    """Host (CPU) tensors, wrong shapes and wrong output buffers are refused
+    before the library is called, so no host pointer reaches a kernel."""
+    import torch
+    from bit_kv_cache_qwm_gb300 import qwm
+    with pytest.raises(ValueError):
+        qwm.qwm_calibrate_static(torch.zeros(2, 64, 128, dtype=torch.bfloat16), 16)
+    with pytest.raises(ValueError):
+        qwm.qwm_kmeans(torch.zeros(2, 300, 128, dtype=torch.bfloat16), torch.zeros(2, 16, dtype=torch.int32), 16)
+    # output dictionary checks run before any device work: a host tensor is refused
+    with pytest.raises(ValueError):
+        qwm._out_tensor(torch.zeros(2, 128), "s", torch.float32, (2, 128), torch.device("cuda", 0))
+    with pytest.raises(ValueError):
+        qwm._device_tensor(torch.zeros(3), "x", (torch.float32,), 1)

@@ -120,7 +120,9 @@ def test_diagnostics_agree_with_oracle(qwm):
     tiles, table = ctx.cache_tiles().cpu().numpy(), ctx.tile_table().cpu().numpy()
     q64, K64, V64 = qn.astype(np.float64), K.double().cpu().numpy(), V.double().cpu().numpy()
     changes, num, den = [], 0.0, 0.0
-    kv = []
+    # the module's reduction: Frobenius norms over all heads together
+    sq = {k: [0.0, 0.0] for k in ("key", "value", "key_only", "value_only", "both")}
+    sig = 1 / np.sqrt(128)
     for i in range(2):
         segs = decode_gpu_segments(tiles[i], table, cent[i], 128, wl.rank, wl.n_centroids, ctx.n_tiles)
         lq = O.compensated_logits(q64[i], segs, {0: U[i]})
@@ -128,11 +130,20 @@ def test_diagnostics_agree_with_oracle(qwm):
         changes.append(np.argmax(ex, axis=1) != np.argmax(lq, axis=1))
         num += ((ex - lq) ** 2).sum()
         den += (ex ** 2).sum()
-        kv.append(O.key_value_study(q64[i], K64[i], V64[i], segs, {0: U[i]}, 1 / np.sqrt(128)))
+        khat = np.concatenate([g.khat for g in segs])
+        vhat = np.concatenate([g.vhat for g in segs])
+        o = O.softmax_rows(ex, sig) @ V64[i]
+        pairs = {"key": (khat, K64[i]), "value": (vhat, V64[i]),
+                 "key_only": (O.softmax_rows(lq, sig) @ V64[i], o),
+                 "value_only": (O.softmax_rows(ex, sig) @ vhat, o),
+                 "both": (O.softmax_rows(lq, sig) @ vhat, o)}
+        for k, (a, b) in pairs.items():
+            sq[k][0] += ((a - b) ** 2).sum()
+            sq[k][1] += (b ** 2).sum()
     want = float(np.mean(np.concatenate(changes)))
     assert abs(got["top1_change"] - want) <= 2.0 / (2 * rows), (got["top1_change"], want)
     assert got["logit_rel_error"] == pytest.approx(np.sqrt(num / den), rel=1e-3)
-    # per-head oracle study vs the module's all-head figures: same order of magnitude
-    for key in ("key_rel_error", "value_rel_error", "output_rel_error_key_only", "output_rel_error_value_only"):
-        lo, hi = min(s[key] for s in kv), max(s[key] for s in kv)
-        assert 0.5 * lo <= got[key] <= 2.0 * hi, (key, got[key], lo, hi)
+    names = {"key": "key_rel_error", "value": "value_rel_error", "key_only": "output_rel_error_key_only",
+             "value_only": "output_rel_error_value_only", "both": "output_rel_error"}
+    for k, key in names.items():
+        assert got[key] == pytest.approx(np.sqrt(sq[k][0] / sq[k][1]), rel=1e-3), key
