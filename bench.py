@@ -191,9 +191,9 @@ def oracle_sample(wl, head=0):
     segs = [O.append_head(synth.keys(wl, ch, [head])[0], synth.values(wl, ch, [head])[0], cent, w, U)
             for ch in range(wl.n_chunks - n_seg, wl.n_chunks)]
     return {"qh": qh, "cent": cent, "w": w, "U": U, "segs": segs, "n_seg": n_seg,
-            "k": synth.keys(wl, last, [head], n=SAMPLE_TOKENS)[0],
-            "v": synth.values(wl, last, [head], n=SAMPLE_TOKENS)[0],
-            "q": synth.queries(wl, last if wl.steps else 0, [head], m=SAMPLE_ROWS)[0]}
+            "k": synth.keys(wl, last, [head], n=min(SAMPLE_TOKENS, wl.chunk))[0],
+            "v": synth.values(wl, last, [head], n=min(SAMPLE_TOKENS, wl.chunk))[0],
+            "q": synth.queries(wl, last if wl.steps else 0, [head], m=min(SAMPLE_ROWS, wl.n_query))[0]}
 
 
 def oracle_step(wl, smp):
