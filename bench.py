@@ -52,8 +52,11 @@ from bit_kv_cache_qwm_gb300 import synth  # noqa: E402
 WORKLOAD = "bf16-h24-stream-n374400"
 METRIC = "qwm_attend TFLOP/s & cache GB/s (% roofline); qwm_append Mtokens/s"
 L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
-KERNEL_IDS = {"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4}
-KERNEL_NAMES = {0: "auto", 1: "simt", 2: "mma", 3: "tcgen05", 4: "tcgen05-2tile", 5: "few-row"}
+KERNEL_IDS = {"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4, "tc3": 6}
+KERNEL_NAMES = {0: "auto", 1: "simt", 2: "mma", 3: "tcgen05", 4: "tcgen05-2tile", 5: "few-row",
+                6: "tcgen05-f16-split"}
+# the committed ncu summary and the source of each large-M attention kernel
+KERNEL_PROFILES = {4: ("attend_tc2_{}.md", "attend_tc.cu"), 6: ("attend_tc3_{}.md", "attend_tc3.cu")}
 
 
 def profiled_traffic(summary, source):
@@ -534,9 +537,10 @@ def run_gpu(args):
                        "attend_kernel": KERNEL_NAMES.get(kern, "?")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],
-                     "traffic": profiled_traffic(os.path.join(ROOT, "profiles", f"attend_tc2_{wl.name}.md"),
-                                                 os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc", "attend_tc.cu"))
-                     if kern == 4 else None,
+                     "traffic": profiled_traffic(os.path.join(ROOT, "profiles", KERNEL_PROFILES[kern][0].format(wl.name)),
+                                                 os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc",
+                                                              KERNEL_PROFILES[kern][1]))
+                     if kern in KERNEL_PROFILES else None,
                      "kernel": "qwm_attend", "peak_source": peaks["source"] + " burst bf16",
                      "work": "H (4 M N d + 2 M N r + 2 M d r) flops per launch"},
         "roofline_append": {"bound": "hbm", "achieved": app_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",

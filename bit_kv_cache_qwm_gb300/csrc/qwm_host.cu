@@ -98,6 +98,12 @@ extern "C" qwm_status qwm_sizes(const qwm_config* c, qwm_layout* out) {
   } else {
     L.st_centroids_f32 = L.st_centroids;
   }
+  if (c->dtype == QWM_BF16 && d == 128) {
+    L.st_centroids_f16 = o;
+    o = align256(o + (size_t)H * c->n_centroids * d * 2);
+  } else {
+    L.st_centroids_f16 = L.st_centroids;
+  }
   L.state_bytes = o;
   L.workspace_bytes = align256(small_workspace_offset(*c) + small_workspace_bytes(*c));
   *out = L;
@@ -135,6 +141,9 @@ extern "C" qwm_status qwm_create(const qwm_config* c, void* d_cache, void* d_sta
   x->energy = (float*)(x->state + L.st_energy);
   x->centroids = (void*)(x->state + L.st_centroids);
   x->cent32 = reinterpret_cast<float*>(x->state + L.st_centroids_f32);
+  x->cent16 = reinterpret_cast<__half*>(x->state + L.st_centroids_f16);
+  x->cent16_flag = x->status + 1;   // the word after the status word
+  x->cent16_ok = false;
   x->basis = (float*)(x->state + L.st_basis);
   x->tiles = (int2*)(x->state + L.st_tiles);
   x->iters = (int32_t*)(x->state + L.st_iters);
@@ -174,17 +183,48 @@ static __global__ void bf16_to_f32_kernel(const __nv_bfloat16* __restrict__ in, 
   if (i < n) out[i] = __bfloat162float(in[i]);
 }
 
+// float16 copy of the bf16 centroids at d = 128 with the channels of every
+// 16-channel block in the order 0, 8, 1, 9, ..., 7, 15 (the operand order of
+// attention kernel 6); a value that rounds beyond the float16 range sets
+// *flag.  bf16 has 8 significant bits, so every centroid inside the range is
+// copied exactly (down to 2^-17; smaller magnitudes round to a multiple of
+// 2^-24).
+static __global__ void bf16_to_f16_blocks_kernel(const __nv_bfloat16* __restrict__ in, __half* __restrict__ out,
+                                                 int64_t n, uint32_t* flag) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int p = (int)(i & 127), q = p & 15;
+  const int ch = (p & ~15) + (q >> 1) + 8 * (q & 1);
+  const __half hv = __float2half_rn(__bfloat162float(in[(i & ~(int64_t)127) + ch]));
+  if (__hisinf(hv)) atomicOr(flag, 1u);
+  out[i] = hv;
+}
+
 extern "C" qwm_status qwm_set_centroids(qwm_ctx* x, const void* d_centroids, void* stream) {
   if (!x || !d_centroids) return QWM_ERR_INVALID_ARG;
   size_t bytes = (size_t)x->cfg.heads * x->cfg.n_centroids * x->cfg.head_dim * x->esz;
   cudaError_t e = cudaMemcpyAsync(x->centroids, d_centroids, bytes, cudaMemcpyDeviceToDevice, S(stream));
+  const int64_t n = (int64_t)x->cfg.heads * x->cfg.n_centroids * x->cfg.head_dim;
   if (e == cudaSuccess && x->cfg.dtype == QWM_BF16) {
-    const int64_t n = (int64_t)x->cfg.heads * x->cfg.n_centroids * x->cfg.head_dim;
     bf16_to_f32_kernel<<<(unsigned)((n + 255) / 256), 256, 0, S(stream)>>>(
         (const __nv_bfloat16*)x->centroids, x->cent32, n);
     e = cudaGetLastError();
   }
+  bool f16_ok = false;
+  if (e == cudaSuccess && x->cfg.dtype == QWM_BF16 && x->cfg.head_dim == 128) {
+    uint32_t flag = 1;
+    e = cudaMemsetAsync(x->cent16_flag, 0, 4, S(stream));
+    if (e == cudaSuccess) {
+      bf16_to_f16_blocks_kernel<<<(unsigned)((n + 255) / 256), 256, 0, S(stream)>>>(
+          (const __nv_bfloat16*)x->centroids, x->cent16, n, x->cent16_flag);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&flag, x->cent16_flag, 4, cudaMemcpyDeviceToHost, S(stream));
+    if (e == cudaSuccess) e = cudaStreamSynchronize(S(stream));
+    f16_ok = e == cudaSuccess && flag == 0;
+  }
   if (e != cudaSuccess) return QWM_ERR_CUDA;
+  x->cent16_ok = f16_ok;
   x->centroids_set = true;
   return QWM_OK;
 }
@@ -316,10 +356,12 @@ extern "C" qwm_status qwm_attend(qwm_ctx* x, const void* d_q, int64_t M, float s
   if (k == 2 && !attend_mma_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 3 && !attend_tc_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 4 && !attend_tc2_supported(x)) return QWM_ERR_UNSUPPORTED;
+  if (k == 6 && !attend_tc3_supported(x)) return QWM_ERR_UNSUPPORTED;
   cudaStream_t s = S(stream);
   cudaError_t e = join_eig(x, s);   // the basis of the last calibration
   if (e != cudaSuccess) return QWM_ERR_CUDA;
   e = k == 5   ? launch_attend_small(x, d_q, M, scale, d_out, x->ws + small_workspace_offset(x->cfg), s)
+      : k == 6 ? launch_attend_tc3(x, d_q, M, scale, d_out, s)
       : k == 4 ? launch_attend_tc2(x, d_q, M, scale, d_out, s)
       : k == 3 ? launch_attend_tc(x, d_q, M, scale, d_out, s)
       : k == 2 ? launch_attend_mma(x, d_q, M, scale, d_out, s)
@@ -376,7 +418,7 @@ extern "C" qwm_status qwm_dequantize(qwm_ctx* x, float* d_khat, float* d_vhat, f
 }
 
 extern "C" qwm_status qwm_set_attend_kernel(qwm_ctx* x, int32_t k) {
-  if (!x || k < 0 || k > 5) return QWM_ERR_INVALID_ARG;
+  if (!x || k < 0 || k > 6) return QWM_ERR_INVALID_ARG;
   x->attend_kernel = k;
   return QWM_OK;
 }
@@ -391,6 +433,7 @@ extern "C" int32_t qwm_attend_kernel_for(const qwm_ctx* x, int64_t M) {
 extern "C" int32_t qwm_resolved_attend_kernel(const qwm_ctx* x) {
   if (!x) return -1;
   if (x->attend_kernel != 0) return x->attend_kernel;
+  if (attend_tc3_supported(x)) return 6;
   if (attend_tc2_supported(x)) return 4;
   if (attend_tc_supported(x)) return 3;
   return attend_mma_supported(x) ? 2 : 1;

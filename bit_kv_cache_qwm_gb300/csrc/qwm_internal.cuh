@@ -43,6 +43,9 @@ struct qwm_ctx {
   float* energy;
   void* centroids;
   float* cent32;    // float32 copy of the centroids (bf16 configs)
+  __half* cent16;   // float16 copy, block channel order 0, 8, 1, 9, ... (bf16, d = 128)
+  uint32_t* cent16_flag;   // device word: a centroid outside the float16 range
+  bool cent16_ok;   // every centroid fits float16 (kernel 6 applies)
   float* basis;     // [max_versions][H][r][d]
   int2* tiles;      // [max_tiles] (version, valid)
   int32_t* iters;   // [H] eigen-solver iterations of the last calibrate
@@ -87,6 +90,9 @@ cudaError_t launch_attend_tc(const qwm_ctx* c, const void* q, int64_t M, float s
 bool attend_tc_supported(const qwm_ctx* c);
 bool attend_tc2_supported(const qwm_ctx* c);
 cudaError_t launch_attend_tc2(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                              cudaStream_t st);
+bool attend_tc3_supported(const qwm_ctx* c);
+cudaError_t launch_attend_tc3(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
                               cudaStream_t st);
 size_t gram_workspace_bytes(const qwm_config& cfg);
 // few-row attention (M <= 64): its workspace follows the calibration's

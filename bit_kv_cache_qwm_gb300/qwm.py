@@ -21,8 +21,9 @@ QWM_F32, QWM_BF16 = 0, 1
 DEV_NOT_CONVERGED, DEV_SATURATED = 0x1, 0x2
 # attention kernels (qwm_set_attend_kernel): automatic choice, float32 SIMT,
 # bf16 mma.sync, tcgen05 with one query tile per CTA, tcgen05 with two query
-# tiles per CTA, few-row split-KV (M <= 64)
-KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA, KERNEL_TC, KERNEL_TC2, KERNEL_SMALL = 0, 1, 2, 3, 4, 5
+# tiles per CTA, few-row split-KV (M <= 64), tcgen05 with the key split into
+# its float16 centroid row and float16 residual
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA, KERNEL_TC, KERNEL_TC2, KERNEL_SMALL, KERNEL_TC3 = 0, 1, 2, 3, 4, 5, 6
 
 STATUS = {0: "QWM_OK", 1: "QWM_ERR_INVALID_ARG", 2: "QWM_ERR_UNSUPPORTED", 3: "QWM_ERR_CAPACITY",
           4: "QWM_ERR_NOT_CALIBRATED", 5: "QWM_ERR_NOT_CONVERGED", 6: "QWM_ERR_CUDA",
@@ -44,7 +45,7 @@ class qwm_layout(ctypes.Structure):
                [(n, ctypes.c_size_t) for n in ("off_idx", "off_kcode", "off_kqp", "off_e", "off_vcode",
                                                 "off_vqp", "st_status", "st_s", "st_w", "st_lambda",
                                                 "st_energy", "st_centroids", "st_basis", "st_tiles",
-                                                "st_iters", "st_centroids_f32")]
+                                                "st_iters", "st_centroids_f32", "st_centroids_f16")]
 
 
 class QwmError(RuntimeError):

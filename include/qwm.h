@@ -93,6 +93,9 @@ typedef struct {
   /* offsets of the arrays inside the state buffer */
   size_t st_status, st_s, st_w, st_lambda, st_energy, st_centroids, st_basis, st_tiles, st_iters;
   size_t st_centroids_f32;  /* float32 copy of bf16 centroids (= st_centroids for f32) */
+  size_t st_centroids_f16;  /* float16 copy of bf16 centroids at d = 128, the channels of
+                               every 16-channel block in the order 0, 8, 1, 9, ..., 7, 15
+                               (= st_centroids when unused)                         */
 } qwm_layout;
 
 typedef struct qwm_ctx qwm_ctx;
@@ -125,7 +128,11 @@ qwm_status qwm_destroy(qwm_ctx* ctx);
 /* Copy the high-precision centroids [H][C][d] (configured dtype, device) into
  * the state.  QSAC chooses among these ("each Key is assigned to a
  * clustering center ... the center retaining high accuracy", roboind
- * article, "Step 1").  Asynchronous on `stream`. */
+ * article, "Step 1").  Asynchronous on `stream`, except for bf16 caches at
+ * d = 128: there the call also builds the float16 copy that attention
+ * kernel 6 reads and waits for `stream` once to learn whether every centroid
+ * fits the float16 range (|C| < 65520); when one does not, kernel 6 is not
+ * used for this context. */
 qwm_status qwm_set_centroids(qwm_ctx* ctx, const void* d_centroids, void* stream);
 
 /* Calibrate from n_h historical queries [H][n_h][d] (device, configured dtype):
@@ -260,21 +267,25 @@ qwm_status qwm_set_assignment(qwm_ctx* ctx, int32_t mode);
 qwm_status qwm_dequantize(qwm_ctx* ctx, float* d_khat, float* d_vhat, float* d_e, void* stream);
 
 /* Attention kernel choice: 0 = automatic (bf16 and d = 128: kernel 5 when
- * M <= 64 and r <= 32, else kernel 4 when r <= 16, kernel 3 when r <= 32;
- * otherwise kernel 2 where it applies, else kernel 1), 1 = float32 CUDA-core
- * kernel, 2 = bf16 mma.sync kernel, 3 = bf16 tcgen05 kernel with 128 query
- * rows per CTA, 4 = bf16 tcgen05 kernel with 256 query rows per CTA
- * (r <= 16), 5 = bf16 kernel for at most 64 query rows (split over the cache
- * tiles, partial results in the context workspace, merged by a second
- * kernel).  An explicit choice the configuration (or M) does not support makes
- * qwm_attend return QWM_ERR_UNSUPPORTED. */
+ * M <= 64 and r <= 32, else kernel 6 when r <= 16 and the centroids fit
+ * float16, kernel 4 when r <= 16, kernel 3 when r <= 32; otherwise kernel 2
+ * where it applies, else kernel 1), 1 = float32 CUDA-core kernel, 2 = bf16
+ * mma.sync kernel, 3 = bf16 tcgen05 kernel with 128 query rows per CTA, 4 =
+ * bf16 tcgen05 kernel with 256 query rows per CTA (r <= 16; the key as two
+ * bf16 terms), 5 = bf16 kernel for at most 64 query rows (split over the
+ * cache tiles, partial results in the context workspace, merged by a second
+ * kernel), 6 = tcgen05 kernel with 256 query rows per CTA and the key split
+ * into its float16 centroid row and float16 residual (r <= 16, centroids
+ * within the float16 range; queries are scaled per row by a power of two
+ * into that range).  An explicit choice the configuration (or M) does not
+ * support makes qwm_attend return QWM_ERR_UNSUPPORTED. */
 qwm_status qwm_set_attend_kernel(qwm_ctx* ctx, int32_t kernel);
 
-/* The attention kernel qwm_attend runs for more than 64 query rows (1 to 4;
- * automatic resolved). */
+/* The attention kernel qwm_attend runs for more than 64 query rows (1 to 4,
+ * or 6; automatic resolved). */
 int32_t qwm_resolved_attend_kernel(const qwm_ctx* ctx);
 
-/* The attention kernel qwm_attend runs for M query rows (1 to 5). */
+/* The attention kernel qwm_attend runs for M query rows (1 to 6). */
 int32_t qwm_attend_kernel_for(const qwm_ctx* ctx, int64_t M);
 
 int64_t qwm_num_tokens(const qwm_ctx* ctx);    /* valid tokens cached        */

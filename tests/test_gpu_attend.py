@@ -117,7 +117,7 @@ def test_full_rank_compensation_on_gpu(qwm, kernel):
     assert np.abs(got - want).max() <= 1e-5 * vmax
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 6])
 def test_attend_bf16_sampled_rows(qwm, kernel):
     """12 heads over 3 appends; the oracle checks every row of heads 0 and 9."""
     name = "bf16-h12-n32760"
@@ -129,7 +129,7 @@ def test_attend_bf16_sampled_rows(qwm, kernel):
     assert np.abs(got[[0, 9]] - want).max() <= 1e-2 * vmax
 
 
-@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4, 6])
 @pytest.mark.parametrize("name,C,r", [("bf16-h12-n32760", 256, 16), ("bf16-h24-append-sweep", 1024, 32),
                                       ("bf16-h24-append-sweep", 64, 8), ("bf16-h24-append-sweep", 256, 0),
                                       ("bf16-h40-n98280-outlier", 256, 16)])
@@ -152,7 +152,7 @@ def test_attend_bf16_variants(qwm, kernel, name, C, r):
             ctx.set_calibration(s_, U)
             bases.append(U)
         ctx.append(_tensor(synth.keys(wl, ch, heads, n), "bf16"), _tensor(synth.values(wl, ch, heads, n), "bf16"))
-    if kernel == 4 and r > 16:
+    if kernel in (4, 6) and r > 16:
         ctx.set_attend_kernel(kernel)
         with pytest.raises(qwm.QwmError) as e:
             ctx.attend(_tensor(synth.queries(wl, 3, heads, m=8), "bf16"))
@@ -175,7 +175,7 @@ def test_attend_full_size_bench_configuration(qwm):
     wl, ctx, cent, bases = _build(qwm, name, list(range(12)), [wl_chunk for wl_chunk in [4680] * 7])
     q = synth.queries(wl, 0)
     got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
-    assert ctx.resolved_attend_kernel == 4
+    assert ctx.resolved_attend_kernel == 6
     rows = np.sort(np.random.default_rng(5).choice(wl.n_query, 48, replace=False))
     qs = q[:, rows]
     want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, qs, [0, 11], 1 / np.sqrt(128))
@@ -184,17 +184,63 @@ def test_attend_full_size_bench_configuration(qwm):
     assert np.isfinite(got).all()
 
 
-@pytest.mark.parametrize("sizes", [[100], [128, 5], [300, 1, 228]])
-def test_attend_two_tile_kernel_split_boundaries(qwm, sizes):
-    """Kernel 4 (256 query rows per CTA) on a cache of one tile (no KV split),
-    two tiles (one tile per split) and five tiles (an odd count split 2 + 3),
-    with M = 300 (two row blocks, the second ragged)."""
+@pytest.mark.parametrize("kernel", [4, 6])
+@pytest.mark.parametrize("sizes", [[100], [128, 5], [300, 1, 228], [64, 65, 1]])
+def test_attend_two_tile_kernel_split_boundaries(qwm, sizes, kernel):
+    """Kernels 4 and 6 (256 query rows per CTA) on a cache of one tile (no
+    KV split), two tiles (one tile per split), five tiles (an odd count split
+    2 + 3) and tiles whose second 64-key half is empty or holds one key, with
+    M = 300 (two row blocks, the second ragged)."""
     name = "bf16-h12-n32760"
     wl, ctx, cent, bases = _build(qwm, name, [0, 1], sizes)
-    ctx.set_attend_kernel(4)
+    ctx.set_attend_kernel(kernel)
     q = synth.queries(wl, 1, [0, 1], m=300)
     got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
     assert ctx.status() == 0
     want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, q, [0, 1], 1 / np.sqrt(128))
     err = np.abs(got - want).max()
     assert err <= 1e-2 * vmax, (err, vmax)
+
+
+def test_attend_f16_split_kernel_large_queries(qwm):
+    """Kernel 6 scales each query row by a power of two into the float16
+    range: rows with entries up to ~2^20 (beyond float16) give the same
+    attention as the oracle (which sees the unscaled bf16 queries)."""
+    name = "bf16-h12-n32760"
+    wl, ctx, cent, bases = _build(qwm, name, [0, 1], [4680, 700])
+    ctx.set_attend_kernel(6)
+    q = synth.queries(wl, 2, [0, 1], m=260)
+    boost = np.ones((1, 260, 1), np.float32)
+    boost[:, ::3] = 2.0 ** 14                       # every third row far beyond float16
+    q = synth.round_to_bf16(q * boost)
+    scale = 1.0 / (np.sqrt(128) * 2.0 ** 13)        # keeps the logits of the boosted rows moderate
+    got = ctx.attend(_tensor(q, "bf16"), scale=scale).float().cpu().numpy()
+    assert ctx.status() == 0 and np.isfinite(got).all()
+    want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, q, [0, 1], scale)
+    err = np.abs(got - want).max()
+    assert err <= 1e-2 * vmax, (err, vmax)
+
+
+def test_attend_centroids_beyond_f16_fall_back(qwm):
+    """Centroids outside the float16 range make kernel 6 unavailable: the
+    automatic choice falls back to kernel 4 (an explicit kernel 6 is refused)
+    and the attention still matches the oracle."""
+    name = "bf16-h12-n32760"
+    wl = synth.workload(name)
+    heads = [0, 1]
+    cent = centroids(name, tuple(heads)).copy()
+    cent[1, 7, 3] = 2.0 ** 17                        # exactly representable in bf16, not in float16
+    ctx = qwm.Qwm(2, 128, wl.rank, wl.n_centroids, dtype="bf16", max_tokens=2 * 128)
+    ctx.set_centroids(_tensor(cent, "bf16"))
+    assert ctx.resolved_attend_kernel == 4
+    s_, U = calibration(name, tuple(heads))
+    ctx.set_calibration(s_, U)
+    ctx.append(_tensor(synth.keys(wl, 0, heads, 200), "bf16"), _tensor(synth.values(wl, 0, heads, 200), "bf16"))
+    q = synth.queries(wl, 0, heads, m=100)
+    got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
+    want, vmax = _oracle_on_gpu_bytes(ctx, cent, [U], q, [0, 1], 1 / np.sqrt(128))
+    assert np.abs(got - want).max() <= 1e-2 * vmax
+    ctx.set_attend_kernel(6)
+    with pytest.raises(qwm.QwmError) as e:
+        ctx.attend(_tensor(q, "bf16"))
+    assert e.value.status == 2

@@ -122,4 +122,4 @@ def test_small_m_kernel_rejects_many_rows(qwm):
     assert e.value.status == 2
     assert ctx.attend_kernel_for(65) == 5          # the explicit choice stands
     ctx.set_attend_kernel(0)
-    assert ctx.attend_kernel_for(65) == 4 and ctx.attend_kernel_for(64) == 5
+    assert ctx.attend_kernel_for(65) == 6 and ctx.attend_kernel_for(64) == 5

@@ -77,7 +77,7 @@ def test_outlier_workload_full_size(qwm):
     assert ctx.n_tokens == wl.n_tokens == 98280
     q = synth.queries(wl, 0)
     got = ctx.attend(_tensor(q)).float().cpu().numpy()
-    assert ctx.resolved_attend_kernel == 4 and ctx.status() == 0
+    assert ctx.resolved_attend_kernel == 6 and ctx.status() == 0
     assert np.isfinite(got).all()
     heads = [0, H - 1]
     _check_rows(ctx, cent, [U], q, got, heads, 16, 7)
@@ -109,6 +109,6 @@ def test_stream_workload_full_size(qwm):
     assert ctx.n_tokens == wl.n_tokens == 374400
     q = synth.queries(wl, wl.n_chunks - 1)
     got = ctx.attend(_tensor(q)).float().cpu().numpy()
-    assert ctx.resolved_attend_kernel == 4 and ctx.status() == 0
+    assert ctx.resolved_attend_kernel == 6 and ctx.status() == 0
     assert np.isfinite(got).all()
     _check_rows(ctx, cent, bases, q, got, [0, H - 1], 16, 11)
