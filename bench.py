@@ -84,6 +84,19 @@ def append_bytes_per_token_head(d, bytes_per_token, in_elem=2):
     return 2 * d * in_elem + bytes_per_token
 
 
+def alu_roofline(token_heads_per_s: float, n_centroids: int, d: int, sms: int, sm_mhz: float) -> dict:
+    """The exhaustive QSAC search does 3 C d float32 operations per
+    token-head (one subtraction, and a max and a min per channel and
+    centroid).  Peak: one scalar float32 operation per lane per cycle on the
+    128 lanes of every SM at the maximum SM clock (packed two-wide adds and
+    three-input min/max can exceed it)."""
+    ops = 3.0 * n_centroids * d
+    peak = 128.0 * sms * sm_mhz * 1e6
+    achieved = token_heads_per_s * ops
+    return {"bound": "alu", "ops_per_token_head": ops, "achieved": achieved / 1e12, "peak": peak / 1e12,
+            "unit": "Tops/s", "frac": achieved / peak}
+
+
 def shard_heads(rank: int, world: int, heads: int) -> list:
     """Global head indices of `rank`'s shard: every rank owns `heads` heads of
     a job of world * heads heads (weak scaling; disjoint shards)."""
@@ -114,8 +127,10 @@ def load_peaks():
         with open(p) as f:
             j = json.load(f)
         return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
-                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "sm_max_mhz": j.get("sm_max_mhz", 2070.0),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0,
+            "source": "fallback"}
 
 
 class ClockSampler:
@@ -550,7 +565,10 @@ def run_gpu(args):
                             "traffic": profiled_traffic(os.path.join(ROOT, "profiles", f"append_{wl.name}.md"),
                                                         os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc",
                                                                      "append.cu")),
-                            "peak_source": peaks["source"] + " HBM copy"},
+                            "peak_source": peaks["source"] + " HBM copy",
+                            "alu": alu_roofline(H * wl.chunk / (app_ms * 1e-3), C, d,
+                                                torch.cuda.get_device_properties(dev).multi_processor_count,
+                                                peaks["sm_max_mhz"])},
         "e2e": {"value": world * flops / (e2e_step * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_step,
                 "copies": "second stream, double-buffered: inputs of step i+1 and output of step i-1 "
@@ -633,7 +651,10 @@ def run_sweep(args):
                            "rank": r, "l2": "flushed between steps (256 MiB write)"},
                 "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": gbs / peaks["hbm_gbs"], "bytes_per_token_head": bpt,
-                             "peak_source": peaks["source"] + " HBM copy"},
+                             "peak_source": peaks["source"] + " HBM copy",
+                             "alu": alu_roofline(world * H * n / (ms * 1e-3), C, d,
+                                                 torch.cuda.get_device_properties(dev).multi_processor_count,
+                                                 peaks["sm_max_mhz"])},
                 "token_heads_per_s": world * H * n / (ms * 1e-3),
                 "gpu_launches": args.steps * (2 if r > 0 else 1), "device_status": int(st)}
         ctx.close()

@@ -59,3 +59,11 @@ def test_whole_job_value_scales_with_replicas():
     one = bench.whole_job_tflops(1e12, 1, 2.0)
     assert bench.whole_job_tflops(1e12, 4, 2.0) == 4 * one
     assert one == 1e12 / 2e-3 / 1e12
+
+
+def test_alu_roofline_of_the_exhaustive_search():
+    """3 C d operations per token-head against 128 lanes x SMs x clock."""
+    r = bench.alu_roofline(1e9, 256, 128, 152, 2070.0)
+    assert r["ops_per_token_head"] == 3 * 256 * 128
+    assert abs(r["peak"] - 128 * 152 * 2070e6 / 1e12) < 1e-9
+    assert abs(r["frac"] - 1e9 * 3 * 256 * 128 / (128 * 152 * 2070e6)) < 1e-12
