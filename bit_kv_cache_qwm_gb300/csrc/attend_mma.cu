@@ -104,6 +104,7 @@ struct MmaArgs {
   int H;
   int r;
   int ib;
+  uint32_t* status;
 };
 
 // RP: e / Z columns after padding (16 or 32); CS: centroids staged in smem
@@ -237,8 +238,9 @@ __global__ void __launch_bounds__(kWarpsA * 32, 1) attend_mma_kernel(const MmaAr
     // ---- dequantise the tile ----
     {
       const int key = tid & 127, half = tid >> 7;
-      const int idx = a.ib == 1 ? tb[a.off.idx + key]
-                                : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
+      const int idx = cent_index(a.ib == 1 ? tb[a.off.idx + key]
+                                           : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key],
+                                 a.nC, a.status);
       const uint4 kc = *reinterpret_cast<const uint4*>(tb + a.off.kcode + key * 32 + half * 16);
       const uint4 vc = *reinterpret_cast<const uint4*>(tb + a.off.vcode + key * 32 + half * 16);
       const uint32_t kw[4] = {kc.x, kc.y, kc.z, kc.w};
@@ -446,6 +448,7 @@ cudaError_t launch_attend_mma(const qwm_ctx* c, const void* q, int64_t M, float 
   a.H = c->cfg.heads;
   a.r = c->cfg.rank;
   a.ib = c->ib;
+  a.status = c->status;
   const int RP = a.r == 0 ? 0 : (a.r <= 16 ? 16 : 32);
   const bool cs = c->cfg.n_centroids <= 256;
   if (RP == 0) return cs ? launch_rp<0, true>(c, a, M, st) : launch_rp<0, false>(c, a, M, st);

@@ -31,7 +31,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 attend_simt_kernel(const T* __restrict__ Q, int64_t M, float scale, T* __restrict__ O,
                    const uint8_t* __restrict__ cache, int64_t max_tiles, TileOffsets off,
                    int64_t n_tiles, const int2* __restrict__ tiles, const T* __restrict__ cent,
-                   int nC, const float* __restrict__ basis, int max_versions, int H, int r, int ib) {
+                   int nC, const float* __restrict__ basis, int max_versions, int H, int r, int ib,
+                   uint32_t* status) {
   constexpr int G = D / kGroup;
   constexpr int J = D / 32;
   extern __shared__ __align__(16) float sm[];
@@ -71,7 +72,7 @@ attend_simt_kernel(const T* __restrict__ Q, int64_t M, float scale, T* __restric
     // ---- dequantise the tile ----
     for (int i = threadIdx.x; i < kTile * G; i += blockDim.x) {
       const int slot = i / G, g = i % G;
-      const int idx = ib == 1 ? tb[off.idx + slot] : reinterpret_cast<const uint16_t*>(tb + off.idx)[slot];
+      const int idx = cent_index(ib == 1 ? tb[off.idx + slot] : reinterpret_cast<const uint16_t*>(tb + off.idx)[slot], nC, status);
       const uint2 kc = *reinterpret_cast<const uint2*>(tb + off.kcode + slot * (D / 4) + g * 8);
       const uint2 vc = *reinterpret_cast<const uint2*>(tb + off.vcode + slot * (D / 4) + g * 8);
       const __half2 kq = *reinterpret_cast<const __half2*>(tb + off.kqp + (slot * G + g) * 4);
@@ -181,7 +182,7 @@ cudaError_t launch_t(const qwm_ctx* c, const void* q, int64_t M, float scale, vo
   kern<<<grid, kWarps * 32, smem, st>>>((const T*)q, M, scale, (T*)out, c->cache, c->lay.max_tiles,
                                         tile_offsets(c->lay), c->n_tiles, c->tiles,
                                         (const T*)c->centroids, c->cfg.n_centroids, c->basis,
-                                        c->cfg.max_versions, c->cfg.heads, r, c->ib);
+                                        c->cfg.max_versions, c->cfg.heads, r, c->ib, c->status);
   return cudaGetLastError();
 }
 

@@ -360,7 +360,8 @@ __global__ void __launch_bounds__(kSmallThreads) attend_small_kernel(const Small
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int key = kb + 2 * t + kk;
-        const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
+        const int idx = cent_index(a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key],
+                                   a.nC, a.status);
         const uint4 qp = *reinterpret_cast<const uint4*>(tb + a.off.kqp + key * G * 4);
         const uint32_t qw[4] = {qp.x, qp.y, qp.z, qp.w};
         float v0 = qcs[g * qld + idx] + se[kk], v1 = qcs[(g + 8) * qld + idx] + se[2 + kk];

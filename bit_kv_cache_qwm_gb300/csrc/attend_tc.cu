@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcArgs a) 
         // ---- k_hat (hi, lo) of 64 keys: thread = (key, 32-channel group) ----
         {
           const int key = hk * 64 + (p >> 2), grp = p & 3;
-          const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
+          const int idx = cent_index(a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key], a.nC, a.status);
           const uint2 kc = *reinterpret_cast<const uint2*>(tb + a.off.kcode + key * 32 + grp * 8);
           const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.kqp + (key * G + grp) * 4);
           const float kz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));
@@ -836,7 +836,7 @@ __global__ void __launch_bounds__(kThreads2, 1) attend_tc2_kernel(const TcArgs a
 #pragma unroll 1
       for (int item = p; item < 512; item += kProdThreads2) {
         const int key = item >> 2, grp = item & 3;
-        const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
+        const int idx = cent_index(a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key], a.nC, a.status);
         const uint2 kc = *reinterpret_cast<const uint2*>(tb + a.off.kcode + key * 32 + grp * 8);
         const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.kqp + (key * G + grp) * 4);
         const float kz = __half2float(__ushort_as_half((unsigned short)(qp & 0xffffu)));

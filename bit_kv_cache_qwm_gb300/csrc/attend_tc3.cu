@@ -390,7 +390,8 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
 #pragma unroll 4
       for (int it = p; it < 2048; it += kProdT) {
         const int key = it >> 4, chunk = it & 15;
-        const int idx = a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key];
+        const int idx = cent_index(a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key],
+                                   a.nC, a.status);
         cp_async16(B1 + op_off(key, chunk), c16 + (int64_t)idx * kD + 8 * chunk);
       }
       cp_async_wait_all();

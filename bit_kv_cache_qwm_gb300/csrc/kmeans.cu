@@ -180,6 +180,7 @@ extern "C" qwm_status qwm_kmeans(int32_t heads, int32_t head_dim, int32_t dtype,
   if (dtype != QWM_F32 && dtype != QWM_BF16) return QWM_ERR_INVALID_ARG;
   if (!d_keys || !d_init_rows || !d_centroids || !d_workspace) return QWM_ERR_INVALID_ARG;
   if ((uintptr_t)d_workspace & 255) return QWM_ERR_INVALID_ARG;
+  if (fault_injected("launch")) return QWM_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = (uint8_t*)d_workspace;
   cudaError_t e;

@@ -120,6 +120,7 @@ extern "C" qwm_status qwm_create(const qwm_config* c, void* d_cache, void* d_sta
   if (!d_cache || !d_state || !d_workspace) return QWM_ERR_INVALID_ARG;
   if (((uintptr_t)d_cache | (uintptr_t)d_state | (uintptr_t)d_workspace) & 255)
     return QWM_ERR_INVALID_ARG;
+  if (fault_injected("oom")) return QWM_ERR_OOM;
   qwm_ctx* x = new (std::nothrow) qwm_ctx();
   if (!x) return QWM_ERR_OOM;
   x->cfg = *c;
@@ -202,6 +203,7 @@ static __global__ void bf16_to_f16_blocks_kernel(const __nv_bfloat16* __restrict
 
 extern "C" qwm_status qwm_set_centroids(qwm_ctx* x, const void* d_centroids, void* stream) {
   if (!x || !d_centroids) return QWM_ERR_INVALID_ARG;
+  if (fault_injected("launch")) return QWM_ERR_CUDA;
   size_t bytes = (size_t)x->cfg.heads * x->cfg.n_centroids * x->cfg.head_dim * x->esz;
   cudaError_t e = cudaMemcpyAsync(x->centroids, d_centroids, bytes, cudaMemcpyDeviceToDevice, S(stream));
   const int64_t n = (int64_t)x->cfg.heads * x->cfg.n_centroids * x->cfg.head_dim;
@@ -248,9 +250,11 @@ static qwm_status next_version(qwm_ctx* x, int32_t* v_out, int32_t* slot_out) {
 
 extern "C" qwm_status qwm_calibrate(qwm_ctx* x, const void* d_q, int64_t n_h, void* stream) {
   if (!x || !d_q || n_h < 1 || n_h > x->cfg.max_hist) return QWM_ERR_INVALID_ARG;
+  NvtxRange range("qwm_calibrate");
   int32_t v, slot;
   qwm_status st = next_version(x, &v, &slot);
   if (st != QWM_OK) return st;
+  if (fault_injected("launch")) return QWM_ERR_CUDA;
   // Gram sums and A^2 on the caller's stream (after the previous
   // eigen-solver has read the buffers this overwrites), then the eigen-solver
   // on the side stream and the group weights on the caller's: the
@@ -279,6 +283,7 @@ extern "C" qwm_status qwm_set_calibration(qwm_ctx* x, const float* h_s, const fl
   int32_t v, slot;
   qwm_status st = next_version(x, &v, &slot);
   if (st != QWM_OK) return st;
+  if (fault_injected("launch")) return QWM_ERR_CUDA;
   const size_t H = x->cfg.heads, d = x->cfg.head_dim, r = x->cfg.rank;
   cudaStream_t s = S(stream);
   cudaError_t e = join_eig(x, s);
@@ -324,6 +329,8 @@ extern "C" qwm_status qwm_append(qwm_ctx* x, const void* d_k, const void* d_v, i
   if (x->version < 0 || !x->centroids_set) return QWM_ERR_NOT_CALIBRATED;
   const int64_t tiles = (n + kTile - 1) / kTile;
   if (x->n_tiles + tiles > x->lay.max_tiles) return QWM_ERR_CAPACITY;
+  if (fault_injected("launch")) return QWM_ERR_CUDA;
+  NvtxRange range("qwm_append");
   // quantisation (group weights only), then the PSAC coefficients once the
   // basis of the current calibration is there
   cudaStream_t s = S(stream);
@@ -357,6 +364,8 @@ extern "C" qwm_status qwm_attend(qwm_ctx* x, const void* d_q, int64_t M, float s
   if (k == 3 && !attend_tc_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 4 && !attend_tc2_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 6 && !attend_tc3_supported(x)) return QWM_ERR_UNSUPPORTED;
+  if (fault_injected("launch")) return QWM_ERR_CUDA;
+  NvtxRange range("qwm_attend");
   cudaStream_t s = S(stream);
   cudaError_t e = join_eig(x, s);   // the basis of the last calibration
   if (e != cudaSuccess) return QWM_ERR_CUDA;
@@ -412,6 +421,7 @@ extern "C" qwm_status qwm_set_assignment(qwm_ctx* x, int32_t mode) {
 extern "C" qwm_status qwm_dequantize(qwm_ctx* x, float* d_khat, float* d_vhat, float* d_e, void* stream) {
   if (!x || !d_khat || !d_vhat || (x->cfg.rank > 0 && !d_e)) return QWM_ERR_INVALID_ARG;
   if (!x->centroids_set) return QWM_ERR_NOT_CALIBRATED;
+  if (fault_injected("launch")) return QWM_ERR_CUDA;
   cudaError_t e = join_eig(x, S(stream));
   if (e == cudaSuccess) e = launch_dequantize(x, d_khat, d_vhat, d_e, S(stream));
   return cuda_status(e);

@@ -5,6 +5,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include <vector>
 
@@ -70,6 +74,27 @@ struct qwm_ctx {
 
 namespace qwm {
 
+// Host-side fault injection for tests of the error paths, read at every call
+// (no GPU fault is involved): QWM_FAULT_INJECT=oom makes qwm_create fail as if
+// the host allocation of the context had failed, before any CUDA call;
+// QWM_FAULT_INJECT=launch makes qwm_set_centroids, qwm_calibrate,
+// qwm_set_calibration, qwm_append, qwm_attend, qwm_dequantize and qwm_kmeans
+// return QWM_ERR_CUDA after their argument checks and before any launch, with
+// the context unchanged.
+inline bool fault_injected(const char* what) {
+  const char* v = getenv("QWM_FAULT_INJECT");
+  return v != nullptr && strcmp(v, what) == 0;
+}
+
+// An NVTX range around one call of the ABI (recorded only when a profiler is
+// attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 // ---- launchers (each returns cudaGetLastError() of its launch) ----
 cudaError_t launch_append(const qwm_ctx* c, const void* k, const void* v, int64_t n,
                           int64_t tile0, int32_t version, cudaStream_t st);
@@ -105,6 +130,23 @@ inline size_t small_workspace_offset(const qwm_config& cfg) {
 }
 
 // ---- device helpers ----
+// The centroid index of a cache slot as read from the cache bytes.  A build
+// with QWM_DEBUG_BOUNDS checks it against the centroid count: an index out of
+// range sets the status bit QWM_DEV_BOUNDS and is replaced by 0, so no read
+// beyond the centroid table follows.  Other builds use it as stored (append
+// writes only indices below the count).
+__device__ __forceinline__ int cent_index(int idx, int nC, uint32_t* status) {
+#ifdef QWM_DEBUG_BOUNDS
+  if ((unsigned)idx >= (unsigned)nC) {
+    atomicOr(status, QWM_DEV_BOUNDS);
+    return 0;
+  }
+#else
+  (void)nC;
+  (void)status;
+#endif
+  return idx;
+}
 __device__ __forceinline__ float load_elem(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float load_elem(const __nv_bfloat16* p, int64_t i) {
   return __bfloat162float(p[i]);

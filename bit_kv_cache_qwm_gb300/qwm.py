@@ -15,10 +15,11 @@ import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libqwm.so")
+# QWM_DEBUG_BOUNDS=1 selects the checking build (build.build(debug_bounds=True))
+LIB_PATH = os.path.join(_PKG, "libqwm_dbg.so" if os.environ.get("QWM_DEBUG_BOUNDS") == "1" else "libqwm.so")
 
 QWM_F32, QWM_BF16 = 0, 1
-DEV_NOT_CONVERGED, DEV_SATURATED = 0x1, 0x2
+DEV_NOT_CONVERGED, DEV_SATURATED, DEV_TIMEOUT, DEV_BOUNDS = 0x1, 0x2, 0x4, 0x8
 # attention kernels (qwm_set_attend_kernel): automatic choice, float32 SIMT,
 # bf16 mma.sync, tcgen05 with one query tile per CTA, tcgen05 with two query
 # tiles per CTA, few-row split-KV (M <= 64), tcgen05 with the key split into
@@ -70,7 +71,7 @@ def lib() -> ctypes.CDLL:
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"libqwm.so not found at {LIB_PATH}: run bit_kv_cache_qwm_gb300/build.py")
+        raise RuntimeError(f"{os.path.basename(LIB_PATH)} not found at {LIB_PATH}: run bit_kv_cache_qwm_gb300/build.py")
     L = ctypes.CDLL(LIB_PATH)
     P, I32, I64, F, VP = ctypes.POINTER, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
     L.qwm_status_string.restype = ctypes.c_char_p

@@ -59,9 +59,26 @@ typedef enum {
 
 typedef enum { QWM_F32 = 0, QWM_BF16 = 1 } qwm_dtype;
 
+/* Test hooks, read from the environment at every call:
+ *   QWM_FAULT_INJECT=oom     qwm_create returns QWM_ERR_OOM after its argument
+ *                            checks, before any CUDA call, creating nothing;
+ *   QWM_FAULT_INJECT=launch  qwm_set_centroids, qwm_calibrate,
+ *                            qwm_set_calibration, qwm_append, qwm_attend,
+ *                            qwm_dequantize and qwm_kmeans return QWM_ERR_CUDA
+ *                            after their argument checks and before launching
+ *                            anything; the context is left unchanged.
+ * A library built with -DQWM_DEBUG_BOUNDS (libqwm_dbg.so) checks every
+ * centroid index it reads from the cache against n_centroids; one out of range
+ * sets QWM_DEV_BOUNDS in the status word and is read as 0.
+ * qwm_calibrate, qwm_append and qwm_attend each open an NVTX range of their
+ * own name (recorded only under a profiler). */
+
 /* device status word bits (qwm_get_status / qwm_peek_status_bits) */
 #define QWM_DEV_NOT_CONVERGED 0x1u  /* calibrate: residual above tolerance at max_iter */
 #define QWM_DEV_SATURATED     0x2u  /* append: a float16 zero or scale saturated at 65504 */
+#define QWM_DEV_TIMEOUT       0x4u  /* a bounded device wait ran out; the kernel left early */
+#define QWM_DEV_BOUNDS        0x8u  /* QWM_DEBUG_BOUNDS builds only: a cache slot named a
+                                       centroid index >= n_centroids (read as 0) */
 
 typedef struct {
   int32_t heads;         /* H >= 1                                              */

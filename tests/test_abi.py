@@ -76,6 +76,23 @@ def test_create_rejects_null_and_misaligned_buffers(qwm):
     assert h.value is None
 
 
+def test_fault_injection_oom_fails_create_before_any_cuda_call(qwm, monkeypatch):
+    """QWM_FAULT_INJECT=oom: qwm_create returns QWM_ERR_OOM after its argument
+    checks and before any CUDA call (so this runs without a GPU: the buffer
+    addresses are never touched), and leaves no context; invalid arguments
+    are still reported as such."""
+    cfg = qwm.make_config(heads=2, head_dim=128, rank=16, n_centroids=256)
+    L = qwm.lib()
+    monkeypatch.setenv("QWM_FAULT_INJECT", "oom")
+    h = ctypes.c_void_p()
+    fake = [ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000), ctypes.c_void_p(0x3000)]
+    assert L.qwm_create(ctypes.byref(cfg), *fake, ctypes.byref(h)) == 7      # QWM_ERR_OOM
+    assert h.value is None
+    assert L.qwm_create(ctypes.byref(cfg), None, None, None, ctypes.byref(h)) == 1
+    monkeypatch.setenv("QWM_FAULT_INJECT", "launch")                      # not a create fault
+    assert L.qwm_create(ctypes.byref(cfg), None, None, None, ctypes.byref(h)) == 1
+
+
 def test_null_context_calls_fail_cleanly(qwm):
     L = qwm.lib()
     assert L.qwm_append(None, None, None, 10, None) == 1
