@@ -7,6 +7,7 @@
 #include <new>
 
 #include "qwm_internal.cuh"
+#include "tcgen05_util.cuh"
 
 using namespace qwm;
 
@@ -170,6 +171,27 @@ extern "C" qwm_status qwm_create(const qwm_config* c, void* d_cache, void* d_sta
   }
   *out = x;
   return QWM_OK;
+}
+
+// One warp waits (the attention kernels' bounded mbarrier wait) on a barrier
+// nothing arrives at: the wait runs out after `limit` SM cycles, sets the
+// timeout bit and the kernel returns.
+__global__ void wait_timeout_kernel(long long limit, uint32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ volatile int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    tcx::bar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  tcx::bar_wait(&bar, 0u, &abort_flag, status, limit);
+}
+
+extern "C" qwm_status qwm_selftest_wait_timeout(int64_t limit_cycles, uint32_t* d_status, void* stream) {
+  if (!d_status || limit_cycles < 1 || limit_cycles > ((int64_t)1 << 32)) return QWM_ERR_INVALID_ARG;
+  wait_timeout_kernel<<<1, 32, 0, S(stream)>>>((long long)limit_cycles, d_status);
+  return cuda_status(cudaGetLastError());
 }
 
 extern "C" qwm_status qwm_destroy(qwm_ctx* ctx) {

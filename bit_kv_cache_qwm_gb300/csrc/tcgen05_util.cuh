@@ -77,7 +77,7 @@ __device__ __forceinline__ void bar_arrive(uint64_t* b) {
 // Bounded wait for the completion of the phase with parity `par`.  Returns
 // false (after flagging) on timeout or when another role already gave up.
 __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t par, volatile int* abort_flag,
-                                         uint32_t* status) {
+                                         uint32_t* status, long long limit = kWaitCycles) {
   const long long t0 = clock64();
   while (true) {
     uint32_t done;
@@ -86,7 +86,7 @@ __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t par, volatile int
                  : "=r"(done) : "r"(su32(b)), "r"(par) : "memory");
     if (done) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(status, kDevTimeout);
       return false;

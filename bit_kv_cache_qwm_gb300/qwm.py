@@ -59,7 +59,7 @@ EXPORTS = ["qwm_status_string", "qwm_sizes", "qwm_create", "qwm_destroy", "qwm_s
            "qwm_calibrate", "qwm_calibrate_static", "qwm_kmeans", "qwm_kmeans_workspace_bytes", "qwm_set_calibration", "qwm_get_calibration", "qwm_append",
            "qwm_attend", "qwm_rewind", "qwm_get_status", "qwm_peek_status_bits",
            "qwm_set_attend_kernel", "qwm_resolved_attend_kernel", "qwm_attend_kernel_for", "qwm_set_assignment",
-           "qwm_dequantize", "qwm_num_tokens",
+           "qwm_dequantize", "qwm_selftest_wait_timeout", "qwm_num_tokens",
            "qwm_num_tiles", "qwm_num_segments", "qwm_version"]
 
 _lib = None
@@ -92,6 +92,7 @@ def lib() -> ctypes.CDLL:
         "qwm_set_attend_kernel": [VP, I32],
         "qwm_set_assignment": [VP, I32],
         "qwm_dequantize": [VP, VP, VP, VP, VP],
+        "qwm_selftest_wait_timeout": [I64, VP, VP],
         "qwm_calibrate_static": [I32, I32, I32, I32, I32, I32, VP, I64, VP, VP, VP, VP, VP, VP],
         "qwm_kmeans": [I32, I32, I32, I32, VP, I64, VP, I32, VP, VP, VP],
     }
@@ -173,6 +174,15 @@ def qwm_calibrate_static(q_hist: torch.Tensor, rank: int, max_iter: int = 64, ov
                                           P(out["U"]), P(out["lambda"]), P(out["energy"]), P(out["status"]),
                                           _stream()), "qwm_calibrate_static")
     return out
+
+
+def selftest_wait_timeout(limit_cycles: int = 1 << 20) -> int:
+    """Run the bounded-wait self-test on the current device and stream and
+    return the status word it leaves (QWM_DEV_TIMEOUT when the wait ran out)."""
+    word = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(lib().qwm_selftest_wait_timeout(int(limit_cycles), ctypes.c_void_p(word.data_ptr()), _stream()),
+           "qwm_selftest_wait_timeout")
+    return int(word.item()) & 0xffffffff
 
 
 def qwm_kmeans(keys: torch.Tensor, init_rows: torch.Tensor, n_centroids: int, iters: int = 25) -> torch.Tensor:

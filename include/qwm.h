@@ -142,6 +142,13 @@ qwm_status qwm_create(const qwm_config* cfg, void* d_cache, void* d_state, void*
  * the context's own stream first.  NULL is a no-op. */
 qwm_status qwm_destroy(qwm_ctx* ctx);
 
+/* Self-test of the bounded device waits: one warp waits on an mbarrier that
+ * nothing arrives at, with the wait of the attention kernels limited to
+ * limit_cycles SM cycles (1 .. 2^32); when it runs out it ORs QWM_DEV_TIMEOUT
+ * into *d_status (a caller-owned, caller-zeroed device word) and the kernel
+ * returns, leaving the CUDA context usable.  Asynchronous on `stream`. */
+qwm_status qwm_selftest_wait_timeout(int64_t limit_cycles, uint32_t* d_status, void* stream);
+
 /* Copy the high-precision centroids [H][C][d] (configured dtype, device) into
  * the state.  QSAC chooses among these ("each Key is assigned to a
  * clustering center ... the center retaining high accuracy", roboind

@@ -90,6 +90,19 @@ def test_oom_fault_on_create(qwm, monkeypatch):
     assert ctx.n_tokens == 0
 
 
+def test_bounded_wait_runs_out_and_the_context_stays_usable(qwm):
+    """A wait on an mbarrier that nothing arrives at (the attention kernels'
+    bounded wait, limited to ~2^20 SM cycles here) gives up, reports
+    QWM_DEV_TIMEOUT in the status word it was handed, and the kernel returns:
+    the CUDA context then runs a full calibrate / append / attend as usual."""
+    assert qwm.selftest_wait_timeout(1 << 20) == qwm.DEV_TIMEOUT
+    name, heads = "bf16-h12-n32760", [0, 1]
+    wl, ctx = _context(qwm, name, heads)
+    ctx.append(_bf16(synth.keys(wl, 0, heads, 300)), _bf16(synth.values(wl, 0, heads, 300)))
+    out = ctx.attend(_bf16(synth.queries(wl, 0, heads, m=100)))
+    assert torch.isfinite(out.float()).all() and ctx.status() == 0
+
+
 _CHILD = r"""
 import sys
 import numpy as np
