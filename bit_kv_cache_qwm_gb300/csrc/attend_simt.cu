@@ -9,9 +9,13 @@
 // A CTA of 8 warps owns 32 query rows of one head; each warp owns 4 rows.
 // Every 128-slot tile is dequantised once per CTA into shared memory
 // (k_hat = centroid + zero + code*scale and v_hat = zero + code*scale in
-// float32, e in the stored float16).  A lane computes the logits of 4 keys with a float64 dot product
-// (products of float32 values are exact in float64), so rounding of the
-// logit stays far below the float32 tolerance of the output; softmax
+// float32, e in the stored float16).  A lane computes the logits of 4 keys
+// with a compensated float32 dot product (Ogita, Rump and Oishi, "Accurate
+// sum and dot product", SIAM J. Sci. Comput. 26(6), 2005, algorithm Dot2:
+// every product split exactly into a float32 pair by a fused multiply-add,
+// the running sum kept with its rounding error), as accurate as a dot product
+// in twice the float32 precision, so rounding of the logit stays far below the
+// float32 tolerance of the output; softmax
 // weights, their sums and the output accumulate in float32 with the running
 // maximum subtracted in float64.  q U_t^T is recomputed whenever the basis
 // version of the tile changes.
@@ -25,6 +29,18 @@ namespace {
 constexpr int kRowsPerWarp = 4;
 constexpr int kWarps = 8;
 constexpr int kRows = kRowsPerWarp * kWarps;
+
+// one term of Dot2: (hi, lo) += x * y, with the product and the sum split
+// exactly (the _rn intrinsics keep the compiler from contracting them)
+__device__ __forceinline__ void dot2_step(float x, float y, float& hi, float& lo) {
+  const float p = __fmul_rn(x, y);
+  const float pe = __fmaf_rn(x, y, -p);          // x * y - p exactly
+  const float s = __fadd_rn(hi, p);
+  const float z = __fsub_rn(s, hi);
+  const float se = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, z)), __fsub_rn(p, z));   // hi + p - s exactly
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(se, pe));
+}
 
 template <int D, typename T>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -116,12 +132,12 @@ attend_simt_kernel(const T* __restrict__ Q, int64_t M, float scale, T* __restric
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int key = lane + 32 * k;
-        double s = 0.0;
+        float hi = 0.f, lo = 0.f;
         const float* kr = kh + key * (D + 1);
-        for (int c = 0; c < D; ++c) s = fma((double)q[c], (double)kr[c], s);
+        for (int c = 0; c < D; ++c) dot2_step(q[c], kr[c], hi, lo);
         const __half* er = es + key * rp;
-        for (int m = 0; m < r; ++m) s = fma((double)z[m], (double)__half2float(er[m]), s);
-        lg[k] = key < nv ? s : -INFINITY;
+        for (int m = 0; m < r; ++m) dot2_step(z[m], __half2float(er[m]), hi, lo);
+        lg[k] = key < nv ? (double)hi + (double)lo : -INFINITY;
         tmax = fmax(tmax, lg[k]);
       }
 #pragma unroll
