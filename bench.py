@@ -52,9 +52,9 @@ from bit_kv_cache_qwm_gb300 import synth  # noqa: E402
 WORKLOAD = "bf16-h24-stream-n374400"
 METRIC = "qwm_attend TFLOP/s & cache GB/s (% roofline); qwm_append Mtokens/s"
 L2_FLUSH_BYTES = 256 << 20   # twice the 129 MB L2
-KERNEL_IDS = {"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4, "tc3": 6}
+KERNEL_IDS = {"auto": 0, "simt": 1, "mma": 2, "tc": 3, "tc2": 4, "tc3": 6, "tc3few": 7}
 KERNEL_NAMES = {0: "auto", 1: "simt", 2: "mma", 3: "tcgen05", 4: "tcgen05-2tile", 5: "few-row",
-                6: "tcgen05-f16-split"}
+                6: "tcgen05-f16-split", 7: "tcgen05-f16-split-few-row"}
 # the committed ncu summary and the source of each large-M attention kernel
 KERNEL_PROFILES = {4: ("attend_tc2_{}.md", "attend_tc.cu"), 6: ("attend_tc3_{}.md", "attend_tc3.cu")}
 

@@ -53,6 +53,7 @@ constexpr int kSmallThreads = kSmallWarps * 32;
 constexpr int kMaxRowBlocks = 4;        // M <= 64
 constexpr int kMaxParts = 64;           // row blocks x splits per head
 constexpr int kPartLd = 132;            // floats per partial row: O[128], m, l, pad
+static_assert(kPartLd == kPartRowFloats, "partial rows shared with the few-row mode of kernel 6");
 constexpr long long kWaitCycles = 1ll << 31;
 constexpr uint32_t kDevTimeout = 0x4u;
 
@@ -638,6 +639,27 @@ size_t small_workspace_bytes(const qwm_config& cfg) {
   const size_t qc = (size_t)cfg.heads * kMaxRowBlocks * 16 * nCp * 4;
   const size_t part = (size_t)cfg.heads * kMaxParts * 16 * kPartLd * 4;
   return ((qc + 255) & ~size_t(255)) + part;
+}
+
+int small_max_parts() { return kMaxParts; }
+
+float* small_part_buffer(const qwm_config& cfg, uint8_t* ws) {
+  const size_t nCp = (cfg.n_centroids + 7) & ~7;
+  const size_t qc_bytes = (size_t)cfg.heads * kMaxRowBlocks * 16 * nCp * 4;
+  return reinterpret_cast<float*>(ws + ((qc_bytes + 255) & ~size_t(255)));
+}
+
+cudaError_t launch_small_combine(const qwm_ctx* c, int64_t M, int n_split, uint8_t* ws, void* out,
+                                 cudaStream_t st) {
+  SmallArgs a = {};
+  a.O = (__nv_bfloat16*)out;
+  a.M = M;
+  a.H = c->cfg.heads;
+  a.n_mb = (int)((M + 15) / 16);
+  a.n_split = n_split;
+  a.part = small_part_buffer(c->cfg, ws);
+  combine_kernel<<<dim3((unsigned)M, a.H), 32, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 bool attend_small_supported(const qwm_ctx* c, int64_t M) {

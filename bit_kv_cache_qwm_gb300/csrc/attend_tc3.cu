@@ -20,7 +20,9 @@
 // order when it is stored.
 //
 // One CTA owns 256 query rows (two M = 128 tiles a, b) of one head and
-// streams its 128-key tiles.  Warp roles (16 warps):
+// streams its 128-key tiles (the few-row mode, kernel 7: one tile of 128
+// rows, the tiles of the cache split over gridDim.z CTAs whose partial
+// results a second kernel merges).  Warp roles (16 warps):
 //   warps 0-3 / 4-7  softmax of query tile a / b: thread = row = TMEM lane.
 //                    Write the row's scaled float16 Q into a SW128 K-major
 //                    shared tile once (the A operand of the S MMAs), then per
@@ -28,12 +30,19 @@
 //                    rescale of O (only when the running maximum grows by
 //                    more than 2^8), P in float16 over the first 64 columns
 //                    of S.
-//   warps 8-14       producers: one thread bulk-copies every packed tile into
-//                    a 2-stage shared ring; per tile all of them gather the
-//                    centroid rows (B1, asynchronous 16-byte copies), then
-//                    write the residuals (B2), the e rows and V_hat, and
-//                    Z = q U_t^T (float16) when a tile's basis slot changes
-//                    (double-buffered, so a basis change never waits).
+//   warps 8-11       key producers, per tile: gather the centroid rows (B1,
+//                    asynchronous 16-byte copies) once the centroid parts of
+//                    the previous tile are done, then write the residuals
+//                    (B2), the e rows and Z = q U_t^T (float16) when a tile's
+//                    basis slot changes (double-buffered, so a basis change
+//                    never waits) once its S MMAs are done.
+//   warps 12-14      value producers: one thread bulk-copies every packed
+//                    tile into a 2-stage shared ring (a stage is refilled
+//                    once both groups are done with it); per tile all write
+//                    V_hat once the previous tile's PV MMAs are done.  The
+//                    two groups run their loops independently, so the value
+//                    dequantisation of a tile overlaps the key work of the
+//                    next.
 //   warp 15          MMA issuer (one lane) and TMEM owner.  Per tile and
 //                    query tile g: S_g = Q_g B1^T (centroid part), then
 //                    S_g += Q_g B2^T + Z_g E^T (residual and PSAC parts),
@@ -62,10 +71,10 @@ using namespace tcx;
 
 constexpr int kD = 128;
 // 16 warps: 4 per SM sub-partition, which leaves 128 registers a thread
-constexpr int kSoftW = 8, kProdW = 7;
-constexpr int kThreads3 = (kSoftW + kProdW + 1) * 32;   // 512
-constexpr int kMmaW = kSoftW + kProdW;                  // 15
-constexpr int kProdT = kProdW * 32;                     // 224
+constexpr int kSoftW = 8, kKeyW = 4, kValW = 3;
+constexpr int kThreads3 = (kSoftW + kKeyW + kValW + 1) * 32;   // 512
+constexpr int kMmaW = kSoftW + kKeyW + kValW;                  // 15
+constexpr int kKeyT = kKeyW * 32, kValT = kValW * 32;          // 128, 96
 constexpr uint32_t kColO = 256;
 // float16 x float16 -> float32, M = 128, N = 128: S (both operands K-major)
 // and PV (MN-major B)
@@ -84,6 +93,7 @@ constexpr int kOffQsc = kOffU + 16 * kD * 4;
 constexpr int kOffZsel = kOffQsc + 256 * 4;
 constexpr int kOffRing = kOffZsel + 64;
 constexpr int kRecvLd = 132;                  // floats per row of a received partial: O[128], m, l, ok, pad
+static_assert(kRecvLd == kPartRowFloats, "the few-row mode writes rows of the combine kernel's partials");
 
 struct Tc3Args {
   const __nv_bfloat16* Q;
@@ -102,14 +112,28 @@ struct Tc3Args {
   int r;
   int ib;
   uint32_t* status;
+  // few-row mode: the KV range split over gridDim.z CTAs (no cluster), each
+  // writing its unnormalised O, running maximum and sum for every row below
+  // M to part[((h n_mb + row / 16) n_split + split) 16 + row % 16][kRecvLd]
+  float* part;
+  int n_mb;
 };
 
-__device__ __forceinline__ void prod_sync3() { asm volatile("bar.sync 1, %0;" ::"n"(kProdT) : "memory"); }
-__device__ __forceinline__ bool prod_all3(bool v) {
+// named barriers of the key producers (1) and the value producers (2)
+__device__ __forceinline__ void key_sync3() { asm volatile("bar.sync 1, %0;" ::"n"(kKeyT) : "memory"); }
+__device__ __forceinline__ void val_sync3() { asm volatile("bar.sync 2, %0;" ::"n"(kValT) : "memory"); }
+__device__ __forceinline__ bool key_all3(bool v) {
   uint32_t r;
   asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, %2, p;\n"
                "selp.u32 %0, 1, 0, q;\n}"
-               : "=r"(r) : "r"((uint32_t)v), "n"(kProdT) : "memory");
+               : "=r"(r) : "r"((uint32_t)v), "n"(kKeyT) : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ bool val_all3(bool v) {
+  uint32_t r;
+  asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 2, %2, p;\n"
+               "selp.u32 %0, 1, 0, q;\n}"
+               : "=r"(r) : "r"((uint32_t)v), "n"(kValT) : "memory");
   return r != 0;
 }
 
@@ -184,7 +208,8 @@ __device__ __forceinline__ float exp_keys(const uint32_t* v, int key0, int nv, f
   return ps.x + ps.y;
 }
 
-template <int RP>
+// NQ: query tiles of 128 rows per CTA (2; 1 in the few-row mode)
+template <int RP, int NQ>
 __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args a) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024 - (su32(sm_raw) & 1023)) & 1023);
@@ -198,7 +223,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
   float* QSC = reinterpret_cast<float*>(sm + kOffQsc);
   volatile int* ZSEL = reinterpret_cast<volatile int*>(sm + kOffZsel);
   uint8_t* Ring = sm + kOffRing;
-  __shared__ __align__(8) uint64_t bars[13];
+  __shared__ __align__(8) uint64_t bars[15];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
   uint64_t* kc_ready = &bars[0];   // centroid rows (B1) of tile t gathered
@@ -210,12 +235,14 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
   uint64_t* pv_done = &bars[8];    // [2] O_g += P_g(t) V(t) done
   uint64_t* full = &bars[10];      // [2] packed tile landed in ring stage
   uint64_t* q_ready = &bars[12];
+  uint64_t* ring_free = &bars[13];  // [2] the key producers are done with the ring stage
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
-  const int64_t row0 = (int64_t)blockIdx.x * 256;
+  const int64_t row0 = (int64_t)blockIdx.x * 128 * NQ;
+  const bool partial = a.part != nullptr;
   const int nsplit = (int)gridDim.z;
-  const int split = nsplit > 1 ? (int)cluster_rank() : 0;
+  const int split = partial ? (int)blockIdx.z : (nsplit > 1 ? (int)cluster_rank() : 0);
   const int t_begin = (int)(a.n_tiles * split / nsplit);
   const int nt = (int)(a.n_tiles * (split + 1) / nsplit) - t_begin;
   float m_run = -INFINITY, l_run = 0.f;      // softmax row state, used by the epilogue
@@ -223,9 +250,11 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
 
   if (tid == 0) {
     abort_sh = 0;
-    bar_init(kc_ready, kProdT);
-    bar_init(kr_ready, kProdT);
-    bar_init(v_ready, kProdT);
+    bar_init(kc_ready, kKeyT);
+    bar_init(kr_ready, kKeyT);
+    bar_init(v_ready, kValT);
+    bar_init(&ring_free[0], 1);
+    bar_init(&ring_free[1], 1);
     bar_init(b1_free, 1);
     for (int g = 0; g < 2; ++g) {
       bar_init(&s_done[g], 1);
@@ -233,7 +262,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       bar_init(&pv_done[g], 1);
       bar_init(&full[g], 1);
     }
-    bar_init(q_ready, 256);
+    bar_init(q_ready, 128 * NQ);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaW) {
@@ -245,7 +274,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
   fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (warp < kSoftW) {
+  if (warp < 4 * NQ) {
     // ------------------------------------------------------------ softmax
     const int g = warp >> 2, i = tid & 127;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -365,30 +394,25 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
     fence_after();
     sm_ok = ok;
-  } else if (warp < kMmaW) {
-    // ------------------------------------------------------------ producers
-    const int p = tid - kSoftW * 32;   // 0..223
+  } else if (warp < kSoftW) {
+    // the softmax warps of a query tile this CTA does not have: idle
+  } else if (warp < kSoftW + kKeyW) {
+    // ------------------------------------------------------------ key producers
+    const int p = tid - kSoftW * 32;   // 0..127
     const uint32_t TB = (uint32_t)a.off.bytes;
-    const uint8_t* tiles_h = a.cache + (int64_t)h * a.max_tiles * a.off.bytes;
     const __half* c16 = a.cent16 + (int64_t)h * a.nC * kD;
     int cur_slot = -1, zb = 1;
     bool ok = true;
-    if (p == 0) {
-      for (int u = 0; u < 2 && u < nt; ++u) {
-        bar_expect_tx(&full[u], TB);
-        bulk_g2s(Ring + u * TB, tiles_h + (int64_t)(t_begin + u) * TB, TB, &full[u]);
-      }
-    }
     // Z needs the per-row scales of Q the softmax warps publish
-    if constexpr (RP > 0) ok = prod_all3(bar_wait(q_ready, 0u, &abort_sh, a.status));
+    if constexpr (RP > 0) ok = key_all3(bar_wait(q_ready, 0u, &abort_sh, a.status));
     for (int t = 0; t < nt && ok; ++t) {
       const uint8_t* tb = Ring + (t & 1) * TB;
       const uint32_t pp = (uint32_t)((t - 1) & 1);
-      if (!prod_all3(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
+      if (!key_all3(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       // ---- B1: the centroid parts of S_a(t-1) and S_b(t-1) have read it
-      if (t > 0 && !prod_all3(bar_wait(b1_free, pp, &abort_sh, a.status))) { ok = false; break; }
+      if (t > 0 && !key_all3(bar_wait(b1_free, pp, &abort_sh, a.status))) { ok = false; break; }
 #pragma unroll 4
-      for (int it = p; it < 2048; it += kProdT) {
+      for (int it = p; it < 2048; it += kKeyT) {
         const int key = it >> 4, chunk = it & 15;
         const int idx = cent_index(a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key],
                                    a.nC, a.status);
@@ -398,8 +422,8 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       fence_async_smem();
       bar_arrive(kc_ready);
       // ---- B2, e, Z: S_a(t-1) and S_b(t-1) are complete
-      if (t > 0 && !prod_all3(bar_wait(&s_done[0], pp, &abort_sh, a.status) &&
-                              bar_wait(&s_done[1], pp, &abort_sh, a.status))) {
+      if (t > 0 && !key_all3(bar_wait(&s_done[0], pp, &abort_sh, a.status) &&
+                              (NQ == 1 || bar_wait(&s_done[1], pp, &abort_sh, a.status)))) {
         ok = false;
         break;
       }
@@ -411,9 +435,9 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
           cur_slot = bslot;
           zb ^= 1;
           const float* Ug = a.basis + ((int64_t)bslot * a.H + h) * a.r * kD;
-          for (int k = p; k < 16 * kD; k += kProdT) US[k] = (k / kD) < a.r ? Ug[k] : 0.f;
-          prod_sync3();
-          for (int zr = p; zr < 256; zr += kProdT) {
+          for (int k = p; k < 16 * kD; k += kKeyT) US[k] = (k / kD) < a.r ? Ug[k] : 0.f;
+          key_sync3();
+          for (int zr = p; zr < 128 * NQ; zr += kKeyT) {
             float z[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) z[k] = 0.f;
@@ -472,7 +496,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
         }
       }
 #pragma unroll 1
-      for (int it = p; it < 1024; it += kProdT) {
+      for (int it = p; it < 1024; it += kKeyT) {
         const int key = it >> 3, b = it & 7;
         const uint32_t w = *reinterpret_cast<const uint32_t*>(tb + a.off.kcode + key * 32 + 4 * b);
         const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.kqp + (key * 4 + (b >> 1)) * 4);
@@ -480,14 +504,34 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       }
       fence_async_smem();
       bar_arrive(kr_ready);
+      // the key producers are done with ring stage t & 1
+      key_sync3();
+      if (p == 0) bar_arrive(&ring_free[t & 1]);
+    }
+  } else if (warp < kMmaW) {
+    // ------------------------------------------------------------ value producers
+    const int p = tid - (kSoftW + kKeyW) * 32;   // 0..95
+    const uint32_t TB = (uint32_t)a.off.bytes;
+    const uint8_t* tiles_h = a.cache + (int64_t)h * a.max_tiles * a.off.bytes;
+    bool ok = true;
+    if (p == 0) {
+      for (int u = 0; u < 2 && u < nt; ++u) {
+        bar_expect_tx(&full[u], TB);
+        bulk_g2s(Ring + u * TB, tiles_h + (int64_t)(t_begin + u) * TB, TB, &full[u]);
+      }
+    }
+    for (int t = 0; t < nt && ok; ++t) {
+      const uint8_t* tb = Ring + (t & 1) * TB;
+      const uint32_t pp = (uint32_t)((t - 1) & 1);
+      if (!val_all3(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       // ---- V_hat: PV_a(t-1) and PV_b(t-1) have read the previous one
-      if (t > 0 && !prod_all3(bar_wait(&pv_done[0], pp, &abort_sh, a.status) &&
-                              bar_wait(&pv_done[1], pp, &abort_sh, a.status))) {
+      if (t > 0 && !val_all3(bar_wait(&pv_done[0], pp, &abort_sh, a.status) &&
+                             (NQ == 1 || bar_wait(&pv_done[1], pp, &abort_sh, a.status)))) {
         ok = false;
         break;
       }
 #pragma unroll 1
-      for (int it = p; it < 1024; it += kProdT) {
+      for (int it = p; it < 1024; it += kValT) {
         const int key = it >> 3, b = it & 7;
         const uint32_t w = *reinterpret_cast<const uint32_t*>(tb + a.off.vcode + key * 32 + 4 * b);
         const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.vqp + (key * 4 + (b >> 1)) * 4);
@@ -495,11 +539,13 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       }
       fence_async_smem();
       bar_arrive(v_ready);
-      // every producer is done with ring stage t & 1: refill it with tile t + 2
-      prod_sync3();
+      // refill ring stage t & 1 with tile t + 2 once both producer groups are done with it
+      val_sync3();
       if (p == 0 && t + 2 < nt) {
-        bar_expect_tx(&full[t & 1], TB);
-        bulk_g2s(Ring + (t & 1) * TB, tiles_h + (int64_t)(t_begin + t + 2) * TB, TB, &full[t & 1]);
+        if (bar_wait(&ring_free[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status)) {
+          bar_expect_tx(&full[t & 1], TB);
+          bulk_g2s(Ring + (t & 1) * TB, tiles_h + (int64_t)(t_begin + t + 2) * TB, TB, &full[t & 1]);
+        }
       }
     }
   } else {
@@ -516,10 +562,10 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       const uint32_t es = su32(Es), zs0 = su32(ZS);
       int n1[2] = {0, 0}, n2[2] = {0, 0}, nP[2] = {0, 0}, nF = 0;
       long long last = clock64();
-      while (nP[0] < nt || nP[1] < nt) {
+      while (nP[0] < nt || (NQ == 2 && nP[1] < nt)) {
         bool did = false;
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < NQ; ++g) {
           const int t = n1[g];
           if (t < nt && nP[g] == t && bar_test(kc_ready, (uint32_t)(t & 1))) {
             fence_after();
@@ -533,12 +579,12 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
             did = true;
           }
         }
-        if (nF < n1[0] && nF < n1[1]) {
+        if (nF < n1[0] && (NQ == 1 || nF < n1[1])) {
           commit(b1_free);
           ++nF;
         }
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < NQ; ++g) {
           const int t = n2[g];
           if (t < n1[g] && bar_test(kr_ready, (uint32_t)(t & 1))) {
             fence_after();
@@ -558,7 +604,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
           }
         }
 #pragma unroll
-        for (int g = 0; g < 2; ++g) {
+        for (int g = 0; g < NQ; ++g) {
           const int t = nP[g];
           if (t < n2[g] && bar_test(&p_ready[g], (uint32_t)(t & 1)) && bar_test(v_ready, (uint32_t)(t & 1))) {
             fence_after();
@@ -586,7 +632,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       // the last PVs complete before the TMEM is released (bounded)
       if (ok && nt > 0) {
         bar_wait(&pv_done[0], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
-        bar_wait(&pv_done[1], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
+        if (NQ == 2) bar_wait(&pv_done[1], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
       }
     }
     __syncwarp();
@@ -601,11 +647,35 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t colO = kColO + 128u * g;
     const int64_t grow = row0 + 128 * g + i;
-    const bool softmax = warp < kSoftW;
+    const bool softmax = warp < 4 * NQ;
     float* recv = reinterpret_cast<float*>(sm) + (128 * g + i) * kRecvLd;   // rank 0's buffers, now free
     float f0 = 1.f, f1 = 0.f, inv = 0.f;
-    bool store = softmax && sm_ok;
-    if (nsplit > 1) {
+    bool store = softmax && sm_ok && !partial;
+    if (partial) {
+      // few-row mode: this split's unnormalised O in channel order, its
+      // running maximum and sum (a split that gave up reports no weight)
+      if (softmax) {
+        float* pr = nullptr;
+        if (grow < a.M)
+          pr = a.part + ((((int64_t)h * a.n_mb + (grow >> 4)) * nsplit + split) * 16 + (grow & 15)) * kRecvLd;
+        for (int cb = 0; cb < 4; ++cb) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + colO + 32 * cb, v);
+          tmem_wait_ld();
+          if (pr) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const int q = k & 15, ch = 16 * (2 * cb + (k >> 4)) + (q >> 1) + 8 * (q & 1);
+              pr[ch] = sm_ok && nt > 0 ? __uint_as_float(v[k]) : 0.f;
+            }
+          }
+        }
+        if (pr) {
+          pr[128] = sm_ok && nt > 0 ? m_run : -INFINITY;
+          pr[129] = sm_ok && nt > 0 ? l_run : 0.f;
+        }
+      }
+    } else if (nsplit > 1) {
       cluster_sync();   // both CTAs are past their tiles
       if (softmax && split == 1) {
         const uint32_t dst = map_rank(su32(recv), 0);
@@ -688,15 +758,42 @@ int tc3_splits(const qwm_ctx* c, int64_t M) {
   return (c->n_tiles >= 2 && w2x2 < 2 * w1) ? 2 : 1;
 }
 
-template <int RP>
-cudaError_t launch_tc3(const qwm_ctx* c, const Tc3Args& a, int64_t M, cudaStream_t st) {
+// few-row mode: KV splits per head, the split count whose CTAs (one per SM)
+// fill 2 to 4 waves best, at most one split per tile and within the
+// partial buffer (row blocks of 16 x splits <= small_max_parts())
+int tc3_few_splits(const qwm_ctx* c, int n_mb) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms < 1)
+    sms = 152;
+  const int64_t units = c->cfg.heads;
+  int64_t cap = small_max_parts() / n_mb;
+  if (cap > c->n_tiles) cap = c->n_tiles;
+  if (cap < 1) cap = 1;
+  int64_t best = 1;
+  double best_fill = -1.0;
+  for (int waves = 2; waves <= 4; ++waves) {
+    int64_t sp = waves * (int64_t)sms / units;
+    if (sp > cap) sp = cap;
+    if (sp < 1) sp = 1;
+    const int64_t ctas = sp * units, used = (ctas + sms - 1) / sms;
+    const double fill = (double)ctas / (double)(used * sms);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = sp;
+    }
+  }
+  return (int)best;
+}
+
+template <int RP, int NQ>
+cudaError_t launch_tc3(const qwm_ctx* c, const Tc3Args& a, int64_t M, int ns, cudaStream_t st) {
   const size_t smem = tc3_smem(c);
-  auto kern = attend_tc3_kernel<RP>;
+  auto kern = attend_tc3_kernel<RP, NQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int ns = tc3_splits(c, M);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((M + 255) / 256), (unsigned)c->cfg.heads, (unsigned)ns);
+  cfg.gridDim = dim3((unsigned)((M + 128 * NQ - 1) / (128 * NQ)), (unsigned)c->cfg.heads, (unsigned)ns);
   cfg.blockDim = dim3(kThreads3, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -706,21 +803,13 @@ cudaError_t launch_tc3(const qwm_ctx* c, const Tc3Args& a, int64_t M, cudaStream
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = (unsigned)ns;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = a.part == nullptr ? 1 : 0;   // the few-row mode's splits meet in the combine kernel
   e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-}  // namespace
-
-bool attend_tc3_supported(const qwm_ctx* c) {
-  return c->cfg.dtype == QWM_BF16 && c->cfg.head_dim == kD && c->cfg.rank <= 16 && c->cent16_ok &&
-         c->lay.max_tiles < (int64_t(1) << 30) && tc3_smem(c) <= 227 * 1024;
-}
-
-cudaError_t launch_attend_tc3(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
-                              cudaStream_t st) {
+Tc3Args tc3_args(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out) {
   Tc3Args a;
   a.Q = (const __nv_bfloat16*)q;
   a.O = (__nv_bfloat16*)out;
@@ -738,7 +827,38 @@ cudaError_t launch_attend_tc3(const qwm_ctx* c, const void* q, int64_t M, float 
   a.r = c->cfg.rank;
   a.ib = c->ib;
   a.status = c->status;
-  return a.r == 0 ? launch_tc3<0>(c, a, M, st) : launch_tc3<16>(c, a, M, st);
+  a.part = nullptr;
+  a.n_mb = 0;
+  return a;
+}
+
+}  // namespace
+
+bool attend_tc3_supported(const qwm_ctx* c) {
+  return c->cfg.dtype == QWM_BF16 && c->cfg.head_dim == kD && c->cfg.rank <= 16 && c->cent16_ok &&
+         c->lay.max_tiles < (int64_t(1) << 30) && tc3_smem(c) <= 227 * 1024;
+}
+
+cudaError_t launch_attend_tc3(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                              cudaStream_t st) {
+  const Tc3Args a = tc3_args(c, q, M, scale, out);
+  const int ns = tc3_splits(c, M);
+  return a.r == 0 ? launch_tc3<0, 2>(c, a, M, ns, st) : launch_tc3<16, 2>(c, a, M, ns, st);
+}
+
+bool attend_tc3_few_supported(const qwm_ctx* c, int64_t M) {
+  return attend_tc3_supported(c) && M >= 1 && M <= 64 && small_workspace_bytes(c->cfg) > 0;
+}
+
+cudaError_t launch_attend_tc3_few(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out, uint8_t* ws,
+                                  cudaStream_t st) {
+  Tc3Args a = tc3_args(c, q, M, scale, out);
+  a.n_mb = (int)((M + 15) / 16);
+  a.part = small_part_buffer(c->cfg, ws);
+  const int ns = tc3_few_splits(c, a.n_mb);
+  cudaError_t e = a.r == 0 ? launch_tc3<0, 1>(c, a, M, ns, st) : launch_tc3<16, 1>(c, a, M, ns, st);
+  if (e != cudaSuccess) return e;
+  return launch_small_combine(c, M, ns, ws, out, st);
 }
 
 }  // namespace qwm

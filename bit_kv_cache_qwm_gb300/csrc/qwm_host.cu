@@ -386,12 +386,14 @@ extern "C" qwm_status qwm_attend(qwm_ctx* x, const void* d_q, int64_t M, float s
   if (k == 3 && !attend_tc_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 4 && !attend_tc2_supported(x)) return QWM_ERR_UNSUPPORTED;
   if (k == 6 && !attend_tc3_supported(x)) return QWM_ERR_UNSUPPORTED;
+  if (k == 7 && !attend_tc3_few_supported(x, M)) return QWM_ERR_UNSUPPORTED;
   if (fault_injected("launch")) return QWM_ERR_CUDA;
   NvtxRange range("qwm_attend");
   cudaStream_t s = S(stream);
   cudaError_t e = join_eig(x, s);   // the basis of the last calibration
   if (e != cudaSuccess) return QWM_ERR_CUDA;
   e = k == 5   ? launch_attend_small(x, d_q, M, scale, d_out, x->ws + small_workspace_offset(x->cfg), s)
+      : k == 7 ? launch_attend_tc3_few(x, d_q, M, scale, d_out, x->ws + small_workspace_offset(x->cfg), s)
       : k == 6 ? launch_attend_tc3(x, d_q, M, scale, d_out, s)
       : k == 4 ? launch_attend_tc2(x, d_q, M, scale, d_out, s)
       : k == 3 ? launch_attend_tc(x, d_q, M, scale, d_out, s)
@@ -450,7 +452,7 @@ extern "C" qwm_status qwm_dequantize(qwm_ctx* x, float* d_khat, float* d_vhat, f
 }
 
 extern "C" qwm_status qwm_set_attend_kernel(qwm_ctx* x, int32_t k) {
-  if (!x || k < 0 || k > 6) return QWM_ERR_INVALID_ARG;
+  if (!x || k < 0 || k > 7) return QWM_ERR_INVALID_ARG;
   x->attend_kernel = k;
   return QWM_OK;
 }

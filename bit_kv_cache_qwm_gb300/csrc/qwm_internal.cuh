@@ -128,6 +128,20 @@ cudaError_t launch_attend_small(const qwm_ctx* c, const void* q, int64_t M, floa
 inline size_t small_workspace_offset(const qwm_config& cfg) {
   return (gram_workspace_bytes(cfg) + 255) & ~size_t(255);
 }
+// the few-row kernels' partial results: rows of kPartRowFloats floats
+// (O[128] unnormalised, running maximum, sum, pad), at most
+// small_max_parts() row blocks x KV splits per head, merged per query row by
+// launch_small_combine
+constexpr int kPartRowFloats = 132;
+int small_max_parts();
+float* small_part_buffer(const qwm_config& cfg, uint8_t* ws);
+cudaError_t launch_small_combine(const qwm_ctx* c, int64_t M, int n_split, uint8_t* ws, void* out,
+                                 cudaStream_t st);
+// kernel 7: kernel 6 with one 128-row query tile per CTA and the KV range
+// split over CTAs (M <= 64), merged by the few-row combine kernel
+bool attend_tc3_few_supported(const qwm_ctx* c, int64_t M);
+cudaError_t launch_attend_tc3_few(const qwm_ctx* c, const void* q, int64_t M, float scale, void* out,
+                                  uint8_t* ws, cudaStream_t st);
 
 // ---- device helpers ----
 // The centroid index of a cache slot as read from the cache bytes.  A build

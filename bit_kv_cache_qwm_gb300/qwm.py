@@ -23,8 +23,10 @@ DEV_NOT_CONVERGED, DEV_SATURATED, DEV_TIMEOUT, DEV_BOUNDS = 0x1, 0x2, 0x4, 0x8
 # attention kernels (qwm_set_attend_kernel): automatic choice, float32 SIMT,
 # bf16 mma.sync, tcgen05 with one query tile per CTA, tcgen05 with two query
 # tiles per CTA, few-row split-KV (M <= 64), tcgen05 with the key split into
-# its float16 centroid row and float16 residual
-KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA, KERNEL_TC, KERNEL_TC2, KERNEL_SMALL, KERNEL_TC3 = 0, 1, 2, 3, 4, 5, 6
+# its float16 centroid row and float16 residual, the same with one query tile
+# per CTA and the cache split over CTAs for M <= 64
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_MMA, KERNEL_TC, KERNEL_TC2, KERNEL_SMALL, KERNEL_TC3, KERNEL_TC3_FEW = \
+    0, 1, 2, 3, 4, 5, 6, 7
 
 STATUS = {0: "QWM_OK", 1: "QWM_ERR_INVALID_ARG", 2: "QWM_ERR_UNSUPPORTED", 3: "QWM_ERR_CAPACITY",
           4: "QWM_ERR_NOT_CALIBRATED", 5: "QWM_ERR_NOT_CONVERGED", 6: "QWM_ERR_CUDA",

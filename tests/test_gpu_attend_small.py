@@ -75,6 +75,52 @@ def test_small_m_variants(qwm, name, C, r, m):
     assert err <= 1e-2 * vmax, (err, vmax)
 
 
+@pytest.mark.parametrize("m", [1, 16, 17, 40, 64])
+@pytest.mark.parametrize("name,C,r", [("bf16-h12-n32760", 256, 16), ("bf16-h24-append-sweep", 1024, 8),
+                                      ("bf16-h24-append-sweep", 256, 0), ("bf16-h24-append-sweep", 7, 3),
+                                      ("bf16-h40-n98280-outlier", 256, 16)])
+def test_few_row_split_key_kernel(qwm, name, C, r, m):
+    """Kernel 7 (kernel 6 with one 128-row query tile per CTA, the cache
+    split over CTAs, partials merged by the few-row combine kernel): ragged
+    appends under three basis versions, rank 0 / 3 / 8 / 16, 7 to 1024
+    centroids, outlier channels, M from 1 to 64."""
+    wl, ctx, cent, bases = _ragged_context(qwm, name, C, r)
+    ctx.set_attend_kernel(7)
+    q = synth.queries(wl, 3, [0, 1], m=m)
+    got = ctx.attend(_tensor(q)).float().cpu().numpy()
+    assert ctx.status() == 0
+    want, vmax = _oracle(ctx, cent, bases, q, [0, 1], 1 / np.sqrt(128))
+    err = np.abs(got - want).max()
+    assert err <= 1e-2 * vmax, (err, vmax)
+
+
+def test_few_row_split_key_kernel_full_cache(qwm):
+    """Kernel 7 over 12 heads x 32,760 cached tokens (259 tiles per head split
+    over many CTAs), 48 rows; the oracle checks heads 0 and 11 completely; an
+    explicit request for more than 64 rows is refused."""
+    name = "bf16-h12-n32760"
+    wl = synth.workload(name)
+    heads = list(range(wl.heads))
+    cent = centroids(name, tuple(heads))
+    ctx = qwm.Qwm(wl.heads, 128, wl.rank, wl.n_centroids, dtype="bf16",
+                  max_tokens=wl.n_chunks * ((wl.chunk + 127) // 128) * 128)
+    ctx.set_centroids(_tensor(cent))
+    s_, U = calibration(name, tuple(heads), wl.rank)
+    ctx.set_calibration(s_, U)
+    for ch in range(wl.n_chunks):
+        ctx.append(_tensor(synth.keys(wl, ch)), _tensor(synth.values(wl, ch)))
+    ctx.set_attend_kernel(7)
+    q = synth.queries(wl, 0, m=48)
+    got = ctx.attend(_tensor(q)).float().cpu().numpy()
+    assert ctx.status() == 0 and np.isfinite(got).all()
+    want, vmax = _oracle(ctx, cent, [U], q, [0, 11], 1 / np.sqrt(128))
+    err = np.abs(got[[0, 11]] - want).max()
+    assert err <= 1e-2 * vmax, (err, vmax)
+    with pytest.raises(qwm.QwmError) as e:
+        ctx.attend(_tensor(synth.queries(wl, 0, m=65)))
+    assert e.value.status == 2
+
+
 def test_small_m_matches_large_m_kernel(qwm):
     """The same 64 rows through kernel 5 and through the tcgen05 kernel agree
     (both within the tolerance of the oracle, and of each other)."""
