@@ -290,10 +290,11 @@ qwm_status qwm_set_assignment(qwm_ctx* ctx, int32_t mode);
  * device buffers.  Asynchronous. */
 qwm_status qwm_dequantize(qwm_ctx* ctx, float* d_khat, float* d_vhat, float* d_e, void* stream);
 
-/* Attention kernel choice: 0 = automatic (bf16 and d = 128: kernel 5 when
- * M <= 64 and r <= 32, else kernel 6 when r <= 16 and the centroids fit
- * float16, kernel 4 when r <= 16, kernel 3 when r <= 32; otherwise kernel 2
- * where it applies, else kernel 1), 1 = float32 CUDA-core kernel, 2 = bf16
+/* Attention kernel choice: 0 = automatic (bf16 and d = 128: for M <= 64 and
+ * r <= 32 kernel 5, or kernel 7 when 32 < M and kernel 6 applies; else kernel
+ * 6 when r <= 16 and the centroids fit float16, kernel 4 when r <= 16, kernel
+ * 3 when r <= 32; otherwise kernel 2 where it applies, else kernel 1), 1 =
+ * float32 CUDA-core kernel, 2 = bf16
  * mma.sync kernel, 3 = bf16 tcgen05 kernel with 128 query rows per CTA, 4 =
  * bf16 tcgen05 kernel with 256 query rows per CTA (r <= 16; the key as two
  * bf16 terms), 5 = bf16 kernel for at most 64 query rows (split over the
@@ -301,15 +302,18 @@ qwm_status qwm_dequantize(qwm_ctx* ctx, float* d_khat, float* d_vhat, float* d_e
  * kernel), 6 = tcgen05 kernel with 256 query rows per CTA and the key split
  * into its float16 centroid row and float16 residual (r <= 16, centroids
  * within the float16 range; queries are scaled per row by a power of two
- * into that range).  An explicit choice the configuration (or M) does not
- * support makes qwm_attend return QWM_ERR_UNSUPPORTED. */
+ * into that range), 7 = kernel 6 with one 128-row query tile per CTA and the
+ * cache tiles split over CTAs, merged by kernel 5's second kernel (M <= 64;
+ * partial results in the context workspace).  An explicit choice the
+ * configuration (or M) does not support makes qwm_attend return
+ * QWM_ERR_UNSUPPORTED. */
 qwm_status qwm_set_attend_kernel(qwm_ctx* ctx, int32_t kernel);
 
 /* The attention kernel qwm_attend runs for more than 64 query rows (1 to 4,
  * or 6; automatic resolved). */
 int32_t qwm_resolved_attend_kernel(const qwm_ctx* ctx);
 
-/* The attention kernel qwm_attend runs for M query rows (1 to 6). */
+/* The attention kernel qwm_attend runs for M query rows (1 to 7). */
 int32_t qwm_attend_kernel_for(const qwm_ctx* ctx, int64_t M);
 
 int64_t qwm_num_tokens(const qwm_ctx* ctx);    /* valid tokens cached        */
