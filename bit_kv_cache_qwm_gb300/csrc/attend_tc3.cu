@@ -119,14 +119,16 @@ struct Tc3Args {
   int n_mb;
 };
 
-// named barriers of the key producers (1) and the value producers (2)
-__device__ __forceinline__ void key_sync3() { asm volatile("bar.sync 1, %0;" ::"n"(kKeyT) : "memory"); }
+// named barriers of the key producers (1; KT threads) and the value producers (2)
+template <int KT>
+__device__ __forceinline__ void key_sync3() { asm volatile("bar.sync 1, %0;" ::"n"(KT) : "memory"); }
 __device__ __forceinline__ void val_sync3() { asm volatile("bar.sync 2, %0;" ::"n"(kValT) : "memory"); }
+template <int KT>
 __device__ __forceinline__ bool key_all3(bool v) {
   uint32_t r;
   asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, %2, p;\n"
                "selp.u32 %0, 1, 0, q;\n}"
-               : "=r"(r) : "r"((uint32_t)v), "n"(kKeyT) : "memory");
+               : "=r"(r) : "r"((uint32_t)v), "n"(KT) : "memory");
   return r != 0;
 }
 __device__ __forceinline__ bool val_all3(bool v) {
@@ -240,6 +242,9 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
   const int64_t row0 = (int64_t)blockIdx.x * 128 * NQ;
+  // key producers: warps 4 NQ .. 11 (with one query tile the second tile's
+  // softmax warps join them)
+  constexpr int KT = kKeyT + 128 * (2 - NQ);
   const bool partial = a.part != nullptr;
   const int nsplit = (int)gridDim.z;
   const int split = partial ? (int)blockIdx.z : (nsplit > 1 ? (int)cluster_rank() : 0);
@@ -250,8 +255,8 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
 
   if (tid == 0) {
     abort_sh = 0;
-    bar_init(kc_ready, kKeyT);
-    bar_init(kr_ready, kKeyT);
+    bar_init(kc_ready, KT);
+    bar_init(kr_ready, KT);
     bar_init(v_ready, kValT);
     bar_init(&ring_free[0], 1);
     bar_init(&ring_free[1], 1);
@@ -394,25 +399,23 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
     fence_after();
     sm_ok = ok;
-  } else if (warp < kSoftW) {
-    // the softmax warps of a query tile this CTA does not have: idle
   } else if (warp < kSoftW + kKeyW) {
     // ------------------------------------------------------------ key producers
-    const int p = tid - kSoftW * 32;   // 0..127
+    const int p = tid - 128 * NQ;   // 0 .. KT - 1
     const uint32_t TB = (uint32_t)a.off.bytes;
     const __half* c16 = a.cent16 + (int64_t)h * a.nC * kD;
     int cur_slot = -1, zb = 1;
     bool ok = true;
     // Z needs the per-row scales of Q the softmax warps publish
-    if constexpr (RP > 0) ok = key_all3(bar_wait(q_ready, 0u, &abort_sh, a.status));
+    if constexpr (RP > 0) ok = key_all3<KT>(bar_wait(q_ready, 0u, &abort_sh, a.status));
     for (int t = 0; t < nt && ok; ++t) {
       const uint8_t* tb = Ring + (t & 1) * TB;
       const uint32_t pp = (uint32_t)((t - 1) & 1);
-      if (!key_all3(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
+      if (!key_all3<KT>(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       // ---- B1: the centroid parts of S_a(t-1) and S_b(t-1) have read it
-      if (t > 0 && !key_all3(bar_wait(b1_free, pp, &abort_sh, a.status))) { ok = false; break; }
+      if (t > 0 && !key_all3<KT>(bar_wait(b1_free, pp, &abort_sh, a.status))) { ok = false; break; }
 #pragma unroll 4
-      for (int it = p; it < 2048; it += kKeyT) {
+      for (int it = p; it < 2048; it += KT) {
         const int key = it >> 4, chunk = it & 15;
         const int idx = cent_index(a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key],
                                    a.nC, a.status);
@@ -422,7 +425,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       fence_async_smem();
       bar_arrive(kc_ready);
       // ---- B2, e, Z: S_a(t-1) and S_b(t-1) are complete
-      if (t > 0 && !key_all3(bar_wait(&s_done[0], pp, &abort_sh, a.status) &&
+      if (t > 0 && !key_all3<KT>(bar_wait(&s_done[0], pp, &abort_sh, a.status) &&
                               (NQ == 1 || bar_wait(&s_done[1], pp, &abort_sh, a.status)))) {
         ok = false;
         break;
@@ -435,9 +438,9 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
           cur_slot = bslot;
           zb ^= 1;
           const float* Ug = a.basis + ((int64_t)bslot * a.H + h) * a.r * kD;
-          for (int k = p; k < 16 * kD; k += kKeyT) US[k] = (k / kD) < a.r ? Ug[k] : 0.f;
-          key_sync3();
-          for (int zr = p; zr < 128 * NQ; zr += kKeyT) {
+          for (int k = p; k < 16 * kD; k += KT) US[k] = (k / kD) < a.r ? Ug[k] : 0.f;
+          key_sync3<KT>();
+          for (int zr = p; zr < 128 * NQ; zr += KT) {
             float z[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) z[k] = 0.f;
@@ -496,7 +499,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
         }
       }
 #pragma unroll 1
-      for (int it = p; it < 1024; it += kKeyT) {
+      for (int it = p; it < 1024; it += KT) {
         const int key = it >> 3, b = it & 7;
         const uint32_t w = *reinterpret_cast<const uint32_t*>(tb + a.off.kcode + key * 32 + 4 * b);
         const uint32_t qp = *reinterpret_cast<const uint32_t*>(tb + a.off.kqp + (key * 4 + (b >> 1)) * 4);
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       fence_async_smem();
       bar_arrive(kr_ready);
       // the key producers are done with ring stage t & 1
-      key_sync3();
+      key_sync3<KT>();
       if (p == 0) bar_arrive(&ring_free[t & 1]);
     }
   } else if (warp < kMmaW) {

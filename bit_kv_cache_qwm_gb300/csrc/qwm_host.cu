@@ -462,8 +462,8 @@ extern "C" int32_t qwm_attend_kernel_for(const qwm_ctx* x, int64_t M) {
   if (x->attend_kernel != 0) return x->attend_kernel;
   // few rows: kernel 5 decodes every tile once per 16-row block, kernel 7
   // once for up to 64 rows at a higher cost per tile; kernel 7 wins from the
-  // third row block on
-  if (attend_small_supported(x, M)) return (M > 32 && attend_tc3_few_supported(x, M)) ? 7 : 5;
+  // second row block on
+  if (attend_small_supported(x, M)) return (M > 16 && attend_tc3_few_supported(x, M)) ? 7 : 5;
   return qwm_resolved_attend_kernel(x);
 }
 

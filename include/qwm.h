@@ -291,7 +291,7 @@ qwm_status qwm_set_assignment(qwm_ctx* ctx, int32_t mode);
 qwm_status qwm_dequantize(qwm_ctx* ctx, float* d_khat, float* d_vhat, float* d_e, void* stream);
 
 /* Attention kernel choice: 0 = automatic (bf16 and d = 128: for M <= 64 and
- * r <= 32 kernel 5, or kernel 7 when 32 < M and kernel 6 applies; else kernel
+ * r <= 32 kernel 5, or kernel 7 when 16 < M and kernel 6 applies; else kernel
  * 6 when r <= 16 and the centroids fit float16, kernel 4 when r <= 16, kernel
  * 3 when r <= 32; otherwise kernel 2 where it applies, else kernel 1), 1 =
  * float32 CUDA-core kernel, 2 = bf16

@@ -66,7 +66,7 @@ def test_small_m_variants(qwm, name, C, r, m):
     rank 0 / 3 / 8 / 16 / 32, 7 to 1024 centroids, outlier channels; M from 1
     to 64 rows (one to four row blocks, ragged)."""
     wl, ctx, cent, bases = _ragged_context(qwm, name, C, r)
-    assert ctx.attend_kernel_for(m) == (7 if m > 32 and r <= 16 else 5)
+    assert ctx.attend_kernel_for(m) == (7 if m > 16 and r <= 16 else 5)
     ctx.set_attend_kernel(5)
     q = synth.queries(wl, 3, [0, 1], m=m)
     got = ctx.attend(_tensor(q)).float().cpu().numpy()
@@ -170,4 +170,4 @@ def test_small_m_kernel_rejects_many_rows(qwm):
     assert ctx.attend_kernel_for(65) == 5          # the explicit choice stands
     ctx.set_attend_kernel(0)
     assert ctx.attend_kernel_for(65) == 6 and ctx.attend_kernel_for(64) == 7
-    assert ctx.attend_kernel_for(33) == 7 and ctx.attend_kernel_for(32) == 5
+    assert ctx.attend_kernel_for(17) == 7 and ctx.attend_kernel_for(16) == 5
