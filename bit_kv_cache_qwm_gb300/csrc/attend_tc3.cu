@@ -43,7 +43,8 @@
 //                    two groups run their loops independently, so the value
 //                    dequantisation of a tile overlaps the key work of the
 //                    next.
-//   warp 15          MMA issuer (one lane) and TMEM owner.  Per tile and
+//   warp 15          MMA issuer and TMEM owner: the warp polls (warp-uniform
+//                    decisions), one elected lane issues.  Per tile and
 //                    query tile g: S_g = Q_g B1^T (centroid part), then
 //                    S_g += Q_g B2^T + Z_g E^T (residual and PSAC parts),
 //                    then O_g += P_g V_hat (A = P in TMEM).  The centroid
@@ -553,14 +554,14 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     }
   } else {
     // ------------------------------------------------------------ MMA issuer
-    const bool leader = lane == 0;
     bool ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
     fence_after();
     // streams per query tile g: the centroid part S1_g(t) (needs B1(t) and
     // PV_g(t-1) issued), the residual part S2_g(t) (needs B2(t) and S1_g(t)
     // issued), PV_g(t) (needs S2_g(t) issued, P_g(t) and V_hat(t)).  The
-    // leader alone polls and issues whatever is ready.
-    if (leader && ok) {
+    // warp polls (warp-uniform decisions, so the descriptors are uniform
+    // values) and one elected lane issues whatever is ready.
+    if (ok) {
       const uint32_t qs0 = su32(Qs), b1 = su32(B1), b2 = su32(B2), vt = su32(Vt);
       const uint32_t es = su32(Es), zs0 = su32(ZS);
       int n1[2] = {0, 0}, n2[2] = {0, 0}, nP[2] = {0, 0}, nF = 0;
@@ -570,38 +571,44 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
           const int t = n1[g];
-          if (t < nt && nP[g] == t && bar_test(kc_ready, (uint32_t)(t & 1))) {
+          if (t < nt && nP[g] == t && warp_all(bar_test(kc_ready, (uint32_t)(t & 1)))) {
             fence_after();
             const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
+            if (elect_one()) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-              mma_ss(d, desc_sw128(qa + ko), desc_sw128(b1 + ko), kIdescS, j > 0);
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+                mma_ss(d, desc_sw128(qa + ko), desc_sw128(b1 + ko), kIdescS, j > 0);
+              }
             }
+            __syncwarp();
             ++n1[g];
             did = true;
           }
         }
         if (nF < n1[0] && (NQ == 1 || nF < n1[1])) {
-          commit(b1_free);
+          if (elect_one()) commit(b1_free);
+          __syncwarp();
           ++nF;
         }
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
           const int t = n2[g];
-          if (t < n1[g] && bar_test(kr_ready, (uint32_t)(t & 1))) {
+          if (t < n1[g] && warp_all(bar_test(kr_ready, (uint32_t)(t & 1)))) {
             fence_after();
             const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
+            const int z = RP > 0 ? ZSEL[0] : 0;
+            if (elect_one()) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-              mma_ss(d, desc_sw128(qa + ko), desc_sw128(b2 + ko), kIdescS, 1);
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+                mma_ss(d, desc_sw128(qa + ko), desc_sw128(b2 + ko), kIdescS, 1);
+              }
+              if constexpr (RP > 0)
+                mma_ss(d, desc_none(zs0 + (z * 2 + g) * kZBuf, 128, 256), desc_none(es, 128, 256), kIdescS, 1);
+              commit(&s_done[g]);
             }
-            if constexpr (RP > 0) {
-              const int z = ZSEL[0];
-              mma_ss(d, desc_none(zs0 + (z * 2 + g) * kZBuf, 128, 256), desc_none(es, 128, 256), kIdescS, 1);
-            }
-            commit(&s_done[g]);
+            __syncwarp();
             ++n2[g];
             did = true;
           }
@@ -609,25 +616,30 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
           const int t = nP[g];
-          if (t < n2[g] && bar_test(&p_ready[g], (uint32_t)(t & 1)) && bar_test(v_ready, (uint32_t)(t & 1))) {
+          if (t < n2[g] && warp_all(bar_test(&p_ready[g], (uint32_t)(t & 1)) && bar_test(v_ready, (uint32_t)(t & 1)))) {
             fence_after();
+            if (elect_one()) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
-                     (t > 0 || j > 0) ? 1u : 0u);
-            commit(&pv_done[g]);
+              for (int j = 0; j < 8; ++j)
+                mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
+                       (t > 0 || j > 0) ? 1u : 0u);
+              commit(&pv_done[g]);
+            }
+            __syncwarp();
             ++nP[g];
             did = true;
           }
         }
         if (did) {
           last = clock64();
-        } else if (abort_sh) {
+        } else if (__any_sync(0xffffffffu, abort_sh != 0)) {
           ok = false;
           break;
-        } else if (clock64() - last > kWaitCycles) {
-          abort_sh = 1;
-          atomicOr(a.status, kDevTimeout);
+        } else if (__any_sync(0xffffffffu, clock64() - last > kWaitCycles)) {
+          if (lane == 0) {
+            abort_sh = 1;
+            atomicOr(a.status, kDevTimeout);
+          }
           ok = false;
           break;
         }

@@ -173,6 +173,14 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// one lane of a fully active warp (the lowest): the lane that issues a
+// warp's MMAs and their commits
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile("{\n.reg .b32 rx;\n.reg .pred px;\nelect.sync rx|px, %1;\n@px mov.s32 %0, 1;\n}"
+               : "+r"(pred) : "r"(0xffffffffu));
+  return pred != 0;
+}
 // warp-uniform result of a bounded wait: tcgen05.ld/st are warp-collective
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
