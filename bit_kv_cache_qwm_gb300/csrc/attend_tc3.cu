@@ -29,7 +29,9 @@
 //                    tile: online softmax in the exp2 domain with a lazy
 //                    rescale of O (only when the running maximum grows by
 //                    more than 2^8), P in float16 over the first 64 columns
-//                    of S.
+//                    of S; once the tile's four warps have written P (a
+//                    128-thread named barrier) the first of them issues
+//                    O_g += P_g V_hat itself and signals the MMA warp.
 //   warps 8-11       key producers, per tile: gather the centroid rows (B1,
 //                    asynchronous 16-byte copies) once the centroid parts of
 //                    the previous tile are done, then write the residuals
@@ -46,8 +48,9 @@
 //   warp 15          MMA issuer and TMEM owner: the warp polls (warp-uniform
 //                    decisions), one elected lane issues.  Per tile and
 //                    query tile g: S_g = Q_g B1^T (centroid part), then
-//                    S_g += Q_g B2^T + Z_g E^T (residual and PSAC parts),
-//                    then O_g += P_g V_hat (A = P in TMEM).  The centroid
+//                    S_g += Q_g B2^T + Z_g E^T (residual and PSAC parts)
+//                    (O_g += P_g V_hat, A = P in TMEM, comes from the
+//                    softmax warps of tile g).  The centroid
 //                    part of the next tile only needs B1, so it runs on the
 //                    tensor pipe while the producers still compute B2.
 //                    S_g(t+1) is issued after PV_g(t), so the tensor pipe's
@@ -124,6 +127,15 @@ struct Tc3Args {
 template <int KT>
 __device__ __forceinline__ void key_sync3() { asm volatile("bar.sync 1, %0;" ::"n"(KT) : "memory"); }
 __device__ __forceinline__ void val_sync3() { asm volatile("bar.sync 2, %0;" ::"n"(kValT) : "memory"); }
+// named barriers of the softmax warps of query tile g (3 + g; 128 threads)
+__device__ __forceinline__ void soft_sync3(int g) { asm volatile("bar.sync %0, 128;" ::"r"(3 + g) : "memory"); }
+__device__ __forceinline__ bool soft_all3(int g, bool v) {
+  uint32_t r;
+  asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, %2, 128, p;\n"
+               "selp.u32 %0, 1, 0, q;\n}"
+               : "=r"(r) : "r"((uint32_t)v), "r"(3 + g) : "memory");
+  return r != 0;
+}
 template <int KT>
 __device__ __forceinline__ bool key_all3(bool v) {
   uint32_t r;
@@ -234,7 +246,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
   uint64_t* v_ready = &bars[2];    // V_hat of tile t written
   uint64_t* b1_free = &bars[3];    // the centroid parts of S_a(t) and S_b(t) done
   uint64_t* s_done = &bars[4];     // [2] S_g(t) complete
-  uint64_t* p_ready = &bars[6];    // [2] P_g(t) written
+  uint64_t* pv_issued = &bars[6];  // [2] PV_g(t) issued (by the softmax warps of tile g)
   uint64_t* pv_done = &bars[8];    // [2] O_g += P_g(t) V(t) done
   uint64_t* full = &bars[10];      // [2] packed tile landed in ring stage
   uint64_t* q_ready = &bars[12];
@@ -264,7 +276,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     bar_init(b1_free, 1);
     for (int g = 0; g < 2; ++g) {
       bar_init(&s_done[g], 1);
-      bar_init(&p_ready[g], 128);
+      bar_init(&pv_issued[g], 1);
       bar_init(&pv_done[g], 1);
       bar_init(&full[g], 1);
     }
@@ -329,7 +341,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     bool ok = true;
     for (int t = 0; t < nt && ok; ++t) {
       const int nv = a.tiles[t_begin + t].y;
-      if (!warp_all(bar_wait(&s_done[g], (uint32_t)(t & 1), &abort_sh, a.status))) { ok = false; break; }
+      if (!soft_all3(g, bar_wait(&s_done[g], (uint32_t)(t & 1), &abort_sh, a.status))) { ok = false; break; }
       fence_after();
       const uint32_t sbase = tmem + lane_base + colS;
       // keys 64-127: their maximum; then keys 0-63, which stay in registers
@@ -395,7 +407,25 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       tmem_wait_st();
       l_run += psum;
       fence_before();
-      bar_arrive(&p_ready[g]);
+      // P_g(t) is complete once the tile's four warps are here; the first of
+      // them issues PV_g(t) itself (no handoff to the MMA warp), then lets
+      // the MMA warp order S_g(t+1) after it
+      soft_sync3(g);
+      if ((warp & 3) == 0) {
+        if (warp_all(bar_wait(v_ready, (uint32_t)(t & 1), &abort_sh, a.status))) {
+          fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(su32(Vt) + 2048 * j), kIdescPV,
+                     (t > 0 || j > 0) ? 1u : 0u);
+            commit(&pv_done[g]);
+          }
+          __syncwarp();
+          fence_before();
+          if (lane == 0) bar_arrive(&pv_issued[g]);
+        }
+      }
     }
     if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
     fence_after();
@@ -557,21 +587,22 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     bool ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
     fence_after();
     // streams per query tile g: the centroid part S1_g(t) (needs B1(t) and
-    // PV_g(t-1) issued), the residual part S2_g(t) (needs B2(t) and S1_g(t)
-    // issued), PV_g(t) (needs S2_g(t) issued, P_g(t) and V_hat(t)).  The
-    // warp polls (warp-uniform decisions, so the descriptors are uniform
-    // values) and one elected lane issues whatever is ready.
+    // PV_g(t-1) issued, by the softmax warps of tile g), the residual part
+    // S2_g(t) (needs B2(t) and S1_g(t) issued).  The warp polls (warp-uniform
+    // decisions, so the descriptors are uniform values) and one elected lane
+    // issues whatever is ready.
     if (ok) {
-      const uint32_t qs0 = su32(Qs), b1 = su32(B1), b2 = su32(B2), vt = su32(Vt);
+      const uint32_t qs0 = su32(Qs), b1 = su32(B1), b2 = su32(B2);
       const uint32_t es = su32(Es), zs0 = su32(ZS);
-      int n1[2] = {0, 0}, n2[2] = {0, 0}, nP[2] = {0, 0}, nF = 0;
+      int n1[2] = {0, 0}, n2[2] = {0, 0}, nF = 0;
       long long last = clock64();
-      while (nP[0] < nt || (NQ == 2 && nP[1] < nt)) {
+      while (n2[0] < nt || (NQ == 2 && n2[1] < nt)) {
         bool did = false;
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
           const int t = n1[g];
-          if (t < nt && nP[g] == t && warp_all(bar_test(kc_ready, (uint32_t)(t & 1)))) {
+          if (t < nt && n2[g] == t && warp_all(bar_test(kc_ready, (uint32_t)(t & 1)) &&
+                                               (t == 0 || bar_test(&pv_issued[g], (uint32_t)((t - 1) & 1))))) {
             fence_after();
             const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
             if (elect_one()) {
@@ -613,23 +644,6 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
             did = true;
           }
         }
-#pragma unroll
-        for (int g = 0; g < NQ; ++g) {
-          const int t = nP[g];
-          if (t < n2[g] && warp_all(bar_test(&p_ready[g], (uint32_t)(t & 1)) && bar_test(v_ready, (uint32_t)(t & 1)))) {
-            fence_after();
-            if (elect_one()) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
-                       (t > 0 || j > 0) ? 1u : 0u);
-              commit(&pv_done[g]);
-            }
-            __syncwarp();
-            ++nP[g];
-            did = true;
-          }
-        }
         if (did) {
           last = clock64();
         } else if (__any_sync(0xffffffffu, abort_sh != 0)) {
@@ -643,11 +657,6 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
           ok = false;
           break;
         }
-      }
-      // the last PVs complete before the TMEM is released (bounded)
-      if (ok && nt > 0) {
-        bar_wait(&pv_done[0], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
-        if (NQ == 2) bar_wait(&pv_done[1], (uint32_t)((nt - 1) & 1), &abort_sh, a.status);
       }
     }
     __syncwarp();
