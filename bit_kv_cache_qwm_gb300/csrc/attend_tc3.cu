@@ -445,12 +445,38 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       if (!key_all3<KT>(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
       // ---- B1: the centroid parts of S_a(t-1) and S_b(t-1) have read it
       if (t > 0 && !key_all3<KT>(bar_wait(b1_free, pp, &abort_sh, a.status))) { ok = false; break; }
-#pragma unroll 4
-      for (int it = p; it < 2048; it += KT) {
-        const int key = it >> 4, chunk = it & 15;
-        const int idx = cent_index(a.ib == 1 ? tb[a.off.idx + key] : reinterpret_cast<const uint16_t*>(tb + a.off.idx)[key],
-                                   a.nC, a.status);
-        cp_async16(B1 + op_off(key, chunk), c16 + (int64_t)idx * kD + 8 * chunk);
+      {
+        // thread: one 16-byte chunk of NK consecutive keys, their indices in
+        // one or two 16-byte loads (a warp covers whole 256-byte centroid rows)
+        constexpr int NK = 2048 / KT;
+        const int chunk = p & 15, k0 = NK * (p >> 4);
+        uint32_t iw[NK / 2];
+        if (a.ib == 1) {
+#pragma unroll
+          for (int q = 0; q < NK / 16 + (NK < 16); ++q) {
+            if constexpr (NK >= 16) {
+              const uint4 w = *reinterpret_cast<const uint4*>(tb + a.off.idx + k0 + 16 * q);
+              iw[4 * q] = w.x, iw[4 * q + 1] = w.y, iw[4 * q + 2] = w.z, iw[4 * q + 3] = w.w;
+            } else {
+              const uint2 w = *reinterpret_cast<const uint2*>(tb + a.off.idx + k0);
+              iw[0] = w.x, iw[1] = w.y;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < NK / 8; ++q) {
+            const uint4 w = *reinterpret_cast<const uint4*>(tb + a.off.idx + 2 * k0 + 16 * q);
+            iw[4 * q] = w.x, iw[4 * q + 1] = w.y, iw[4 * q + 2] = w.z, iw[4 * q + 3] = w.w;
+          }
+        }
+        const __half* csrc = c16 + 8 * chunk;
+#pragma unroll
+        for (int k = 0; k < NK; ++k) {
+          const int raw = a.ib == 1 ? (int)((iw[k >> 2] >> (8 * (k & 3))) & 0xffu)
+                                    : (int)((iw[k >> 1] >> (16 * (k & 1))) & 0xffffu);
+          const int idx = cent_index(raw, a.nC, a.status);
+          cp_async16(B1 + op_off(k0 + k, chunk), csrc + (int64_t)idx * kD);
+        }
       }
       cp_async_wait_all();
       fence_async_smem();
