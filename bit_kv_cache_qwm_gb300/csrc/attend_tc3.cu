@@ -198,7 +198,8 @@ __device__ __forceinline__ float bf16_at(const uint4* x, int ch) {
 // online-softmax step of one row over the 16 Q keys key0 .. key0 + 16 Q - 1
 // of a tile held in v[0 .. 16 Q - 1]: P (float16 pairs) into TMEM columns
 // key0 / 2 .. of the row's S buffer; returns the sum of the P values
-template <int Q>
+// (FULL: all 128 keys of the tile are valid, no per-key test)
+template <int Q, bool FULL>
 __device__ __forceinline__ float exp_keys(const uint32_t* v, int key0, int nv, float2 c2v, float2 mv,
                                           uint32_t taddr) {
   float2 ps = make_float2(0.f, 0.f);
@@ -210,7 +211,7 @@ __device__ __forceinline__ float exp_keys(const uint32_t* v, int key0, int nv, f
       const int k0 = 16 * q + 2 * k, key = key0 + k0;
       const float2 arg = __ffma2_rn(make_float2(__uint_as_float(v[k0]), __uint_as_float(v[k0 + 1])), c2v, mv);
       float2 pp = make_float2(ex2(arg.x), ex2(arg.y));
-      if (nv < 128) {
+      if (!FULL) {
         pp.x = key < nv ? pp.x : 0.f;
         pp.y = key + 1 < nv ? pp.y : 0.f;
       }
@@ -396,13 +397,14 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       // keys 0-63 first (they are in registers; their P goes over S columns
       // 0-31, already read), then keys 64-127 again from TMEM (S columns
       // 64-127, untouched), whose P goes over columns 32-63
-      float psum = exp_keys<4>(v, 0, nv, c2v, mv, sbase);
+      float psum = nv >= 128 ? exp_keys<4, true>(v, 0, nv, c2v, mv, sbase) : exp_keys<4, false>(v, 0, nv, c2v, mv, sbase);
 #pragma unroll 1
       for (int hq = 0; hq < 2; ++hq) {
         uint32_t w[32];
         tmem_ld32(sbase + 64 + 32 * hq, w);
         tmem_wait_ld();
-        psum += exp_keys<2>(w, 64 + 32 * hq, nv, c2v, mv, sbase);
+        psum += nv >= 128 ? exp_keys<2, true>(w, 64 + 32 * hq, nv, c2v, mv, sbase)
+                          : exp_keys<2, false>(w, 64 + 32 * hq, nv, c2v, mv, sbase);
       }
       tmem_wait_st();
       l_run += psum;
