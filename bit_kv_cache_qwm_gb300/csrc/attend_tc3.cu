@@ -127,6 +127,17 @@ struct Tc3Args {
 template <int KT>
 __device__ __forceinline__ void key_sync3() { asm volatile("bar.sync 1, %0;" ::"n"(KT) : "memory"); }
 __device__ __forceinline__ void val_sync3() { asm volatile("bar.sync 2, %0;" ::"n"(kValT) : "memory"); }
+// named barriers "V_hat of the tile written" for query tile g (5 + g): the
+// value producers arrive, the warp of tile g that issues PV_g waits.  A named
+// barrier does not pass through the shared-memory pipe, which the MMAs'
+// operand reads and the producers' stores keep busy, so the handoff costs
+// tens of cycles instead of hundreds.
+__device__ __forceinline__ void vready_arrive(int g) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(5 + g), "n"(kValT + 32) : "memory");
+}
+__device__ __forceinline__ void vready_sync(int g) {
+  asm volatile("bar.sync %0, %1;" ::"r"(5 + g), "n"(kValT + 32) : "memory");
+}
 // named barriers of the softmax warps of query tile g (3 + g; 128 threads)
 __device__ __forceinline__ void soft_sync3(int g) { asm volatile("bar.sync %0, 128;" ::"r"(3 + g) : "memory"); }
 __device__ __forceinline__ bool soft_all3(int g, bool v) {
@@ -244,7 +255,6 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
   __shared__ volatile int abort_sh;
   uint64_t* kc_ready = &bars[0];   // centroid rows (B1) of tile t gathered
   uint64_t* kr_ready = &bars[1];   // residuals (B2), e (and Z) of tile t written
-  uint64_t* v_ready = &bars[2];    // V_hat of tile t written
   uint64_t* b1_free = &bars[3];    // the centroid parts of S_a(t) and S_b(t) done
   uint64_t* s_done = &bars[4];     // [2] S_g(t) complete
   uint64_t* pv_issued = &bars[6];  // [2] PV_g(t) issued (by the softmax warps of tile g)
@@ -271,7 +281,6 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     abort_sh = 0;
     bar_init(kc_ready, KT);
     bar_init(kr_ready, KT);
-    bar_init(v_ready, kValT);
     bar_init(&ring_free[0], 1);
     bar_init(&ring_free[1], 1);
     bar_init(b1_free, 1);
@@ -414,19 +423,20 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       // the MMA warp order S_g(t+1) after it
       soft_sync3(g);
       if ((warp & 3) == 0) {
-        if (warp_all(bar_wait(v_ready, (uint32_t)(t & 1), &abort_sh, a.status))) {
-          fence_after();
-          if (elect_one()) {
+        // V_hat(t) is written once the value producers have arrived (they
+        // arrive once more if they give up, so this never waits forever)
+        vready_sync(g);
+        fence_after();
+        if (elect_one()) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(su32(Vt) + 2048 * j), kIdescPV,
-                     (t > 0 || j > 0) ? 1u : 0u);
-            commit(&pv_done[g]);
-          }
-          __syncwarp();
-          fence_before();
-          if (lane == 0) bar_arrive(&pv_issued[g]);
+          for (int j = 0; j < 8; ++j)
+            mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(su32(Vt) + 2048 * j), kIdescPV,
+                   (t > 0 || j > 0) ? 1u : 0u);
+          commit(&pv_done[g]);
         }
+        __syncwarp();
+        fence_before();
+        if (lane == 0) bar_arrive(&pv_issued[g]);
       }
     }
     if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
@@ -600,7 +610,8 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
         dq_block(Vt, key, b, w, qp);
       }
       fence_async_smem();
-      bar_arrive(v_ready);
+      vready_arrive(0);
+      if (NQ == 2) vready_arrive(1);
       // refill ring stage t & 1 with tile t + 2 once both producer groups are done with it
       val_sync3();
       if (p == 0 && t + 2 < nt) {
@@ -609,6 +620,12 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
           bulk_g2s(Ring + (t & 1) * TB, tiles_h + (int64_t)(t_begin + t + 2) * TB, TB, &full[t & 1]);
         }
       }
+    }
+    // a group that gave up before arriving for its current tile arrives once
+    // more, so that a softmax warp waiting for that tile's V_hat is released
+    if (!ok) {
+      vready_arrive(0);
+      if (NQ == 2) vready_arrive(1);
     }
   } else {
     // ------------------------------------------------------------ MMA issuer
