@@ -45,24 +45,31 @@
 //                    two groups run their loops independently, so the value
 //                    dequantisation of a tile overlaps the key work of the
 //                    next.
-//   warp 15          MMA issuer and TMEM owner: the warp polls (warp-uniform
-//                    decisions), one elected lane issues.  Per tile and
-//                    query tile g: S_g = Q_g B1^T (centroid part), then
-//                    S_g += Q_g B2^T + Z_g E^T (residual and PSAC parts)
-//                    (O_g += P_g V_hat, A = P in TMEM, comes from the
-//                    softmax warps of tile g).  The centroid
-//                    part of the next tile only needs B1, so it runs on the
-//                    tensor pipe while the producers still compute B2.
-//                    S_g(t+1) is issued after PV_g(t), so the tensor pipe's
-//                    in-order execution keeps P_g(t) intact until PV_g(t)
-//                    has read it.
+//   warp 15          MMA issuer and TMEM owner: per tile, in a fixed order,
+//                    S_a = Q_a B1^T, S_b = Q_b B1^T (centroid parts), then
+//                    S_g += Q_g B2^T + Z_g E^T (residual and PSAC parts); the
+//                    whole warp waits, one elected lane issues (O_g += P_g
+//                    V_hat, A = P in TMEM, comes from the softmax warps of
+//                    tile g).  The centroid part of the next tile only needs
+//                    B1, so it runs on the tensor pipe while the producers
+//                    still compute B2.  S_g(t+1) is issued after PV_g(t), so
+//                    the tensor pipe's in-order execution keeps P_g(t) intact
+//                    until PV_g(t) has read it.
+// Handoffs between threads (V_hat written, B1 gathered, B2 written, PV issued)
+// use named barriers: an mbarrier wait goes through the shared-memory pipe,
+// which the MMAs' operand reads and the producers' stores keep busy (a wait
+// on a completed mbarrier then takes hundreds of cycles).  The tensor pipe's
+// completions (S done, PV done, B1 free) arrive on mbarriers.
 // TMEM columns: S_a [0,128), S_b [128,256), O_a [256,384), O_b [384,512).
 // Split KV: with gridDim.z = 2 the two CTAs of a cluster take the two halves
 // of the tile range for the same rows; rank 1 sends its unnormalised O,
 // running maximum and sum to rank 0 through distributed shared memory and
 // rank 0 merges them (log-sum-exp).
-// Every wait is bounded by the SM clock; a timeout sets a device status bit
-// and every role leaves its loop, the TMEM is freed and the kernel returns.
+// Every mbarrier wait is bounded by the SM clock; a timeout sets a device
+// status bit and every role leaves its loop (a role that leaves arrives once
+// more on the named barriers it feeds, and a role that waits on one reads the
+// abort flag after each wait and stops before the next), the TMEM is freed
+// and the kernel returns.
 #include <math.h>
 
 #include "qwm_internal.cuh"
@@ -138,6 +145,15 @@ __device__ __forceinline__ void vready_arrive(int g) {
 __device__ __forceinline__ void vready_sync(int g) {
   asm volatile("bar.sync %0, %1;" ::"r"(5 + g), "n"(kValT + 32) : "memory");
 }
+// The MMA warp's inputs arrive on named barriers too: "PV_g issued" (7 + g;
+// the PV-issuing softmax warp of tile g arrives), "B1 gathered" (9) and "B2,
+// e, Z written" (10; the key producers arrive).  Whoever arrives does so once
+// per tile, and once more for the tile it was on if it gives up; the MMA warp
+// reads the abort flag after each tile's last wait and stops at the next, so
+// no named-barrier wait is left without its arrival.
+constexpr int kNbPvi = 7, kNbKc = 9, kNbKr = 10;
+__device__ __forceinline__ void nbar_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void nbar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 // named barriers of the softmax warps of query tile g (3 + g; 128 threads)
 __device__ __forceinline__ void soft_sync3(int g) { asm volatile("bar.sync %0, 128;" ::"r"(3 + g) : "memory"); }
 __device__ __forceinline__ bool soft_all3(int g, bool v) {
@@ -248,22 +264,18 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
   uint8_t* ZS = sm + kOffZ;
   float* US = reinterpret_cast<float*>(sm + kOffU);
   float* QSC = reinterpret_cast<float*>(sm + kOffQsc);
-  volatile int* ZSEL = reinterpret_cast<volatile int*>(sm + kOffZsel);
   uint8_t* Ring = sm + kOffRing;
   __shared__ __align__(8) uint64_t bars[15];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_sh;
-  uint64_t* kc_ready = &bars[0];   // centroid rows (B1) of tile t gathered
-  uint64_t* kr_ready = &bars[1];   // residuals (B2), e (and Z) of tile t written
   uint64_t* b1_free = &bars[3];    // the centroid parts of S_a(t) and S_b(t) done
   uint64_t* s_done = &bars[4];     // [2] S_g(t) complete
-  uint64_t* pv_issued = &bars[6];  // [2] PV_g(t) issued (by the softmax warps of tile g)
   uint64_t* pv_done = &bars[8];    // [2] O_g += P_g(t) V(t) done
   uint64_t* full = &bars[10];      // [2] packed tile landed in ring stage
   uint64_t* q_ready = &bars[12];
   uint64_t* ring_free = &bars[13];  // [2] the key producers are done with the ring stage
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int h = blockIdx.y;
   const int64_t row0 = (int64_t)blockIdx.x * 128 * NQ;
   // key producers: warps 4 NQ .. 11 (with one query tile the second tile's
@@ -279,14 +291,11 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
 
   if (tid == 0) {
     abort_sh = 0;
-    bar_init(kc_ready, KT);
-    bar_init(kr_ready, KT);
     bar_init(&ring_free[0], 1);
     bar_init(&ring_free[1], 1);
     bar_init(b1_free, 1);
     for (int g = 0; g < 2; ++g) {
       bar_init(&s_done[g], 1);
-      bar_init(&pv_issued[g], 1);
       bar_init(&pv_done[g], 1);
       bar_init(&full[g], 1);
     }
@@ -348,8 +357,9 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       fence_async_smem();
       bar_arrive(q_ready);
     }
-    bool ok = true;
-    for (int t = 0; t < nt && ok; ++t) {
+    bool ok = true, pv_ab = false;
+    int ab_read = 0, t = 0;
+    for (; t < nt && ok; ++t) {
       const int nv = a.tiles[t_begin + t].y;
       if (!soft_all3(g, bar_wait(&s_done[g], (uint32_t)(t & 1), &abort_sh, a.status))) { ok = false; break; }
       fence_after();
@@ -424,21 +434,29 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       soft_sync3(g);
       if ((warp & 3) == 0) {
         // V_hat(t) is written once the value producers have arrived (they
-        // arrive once more if they give up, so this never waits forever)
-        vready_sync(g);
-        fence_after();
-        if (elect_one()) {
+        // arrive once more if they give up; once the abort flag, read after
+        // the previous wait, is set, this warp waits no more)
+        pv_ab = pv_ab || __any_sync(0xffffffffu, ab_read != 0);
+        if (!pv_ab) {
+          vready_sync(g);
+          ab_read = abort_sh;
+          fence_after();
+          if (elect_one()) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(su32(Vt) + 2048 * j), kIdescPV,
-                   (t > 0 || j > 0) ? 1u : 0u);
-          commit(&pv_done[g]);
+            for (int j = 0; j < 8; ++j)
+              mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(su32(Vt) + 2048 * j), kIdescPV,
+                     (t > 0 || j > 0) ? 1u : 0u);
+            commit(&pv_done[g]);
+          }
+          __syncwarp();
         }
-        __syncwarp();
         fence_before();
-        if (lane == 0) bar_arrive(&pv_issued[g]);
+        if (t + 1 < nt) nbar_arrive(kNbPvi + g, 64);
       }
     }
+    // a group that gave up before issuing PV_g(t) still lets the MMA warp pass
+    // its wait for it
+    if (!ok && (warp & 3) == 0 && t + 1 < nt) nbar_arrive(kNbPvi + g, 64);
     if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
     fence_after();
     sm_ok = ok;
@@ -450,8 +468,10 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     int cur_slot = -1, zb = 1;
     bool ok = true;
     // Z needs the per-row scales of Q the softmax warps publish
+    bool kc_due = true;   // the tile's "B1 gathered" arrival is still due
     if constexpr (RP > 0) ok = key_all3<KT>(bar_wait(q_ready, 0u, &abort_sh, a.status));
     for (int t = 0; t < nt && ok; ++t) {
+      kc_due = true;
       const uint8_t* tb = Ring + (t & 1) * TB;
       const uint32_t pp = (uint32_t)((t - 1) & 1);
       if (!key_all3<KT>(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
@@ -492,7 +512,8 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       }
       cp_async_wait_all();
       fence_async_smem();
-      bar_arrive(kc_ready);
+      nbar_arrive(kNbKc, KT + 32);
+      kc_due = false;
       // ---- B2, e, Z: S_a(t-1) and S_b(t-1) are complete
       if (t > 0 && !key_all3<KT>(bar_wait(&s_done[0], pp, &abort_sh, a.status) &&
                               (NQ == 1 || bar_wait(&s_done[1], pp, &abort_sh, a.status)))) {
@@ -542,7 +563,6 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
             }
           }
         }
-        if (p == 0) ZSEL[0] = zb;
         if (p < 128) {
           // e row of key p: r float16 values, zero-padded to 16, as two core
           // matrices of a no-swizzle K-major tile
@@ -575,10 +595,15 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
         dq_block(B2, key, b, w, qp);
       }
       fence_async_smem();
-      bar_arrive(kr_ready);
+      nbar_arrive(kNbKr, KT + 32);
       // the key producers are done with ring stage t & 1
       key_sync3<KT>();
       if (p == 0) bar_arrive(&ring_free[t & 1]);
+    }
+    // a group that gave up arrives once more for the tile it was on
+    if (!ok && nt > 0) {
+      if (kc_due) nbar_arrive(kNbKc, KT + 32);
+      nbar_arrive(kNbKr, KT + 32);
     }
   } else if (warp < kMmaW) {
     // ------------------------------------------------------------ value producers
@@ -631,76 +656,62 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     // ------------------------------------------------------------ MMA issuer
     bool ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
     fence_after();
-    // streams per query tile g: the centroid part S1_g(t) (needs B1(t) and
-    // PV_g(t-1) issued, by the softmax warps of tile g), the residual part
-    // S2_g(t) (needs B2(t) and S1_g(t) issued).  The warp polls (warp-uniform
-    // decisions, so the descriptors are uniform values) and one elected lane
-    // issues whatever is ready.
+    // per tile, in a fixed order: the centroid parts S1_a(t), S1_b(t) (B1(t)
+    // gathered, PV_g(t-1) issued by the softmax warps of tile g), then the
+    // residual and PSAC parts S2_a(t), S2_b(t) (B2(t), e and Z written).  All
+    // waits are named barriers; the whole warp waits, one elected lane issues.
     if (ok) {
       const uint32_t qs0 = su32(Qs), b1 = su32(B1), b2 = su32(B2);
       const uint32_t es = su32(Es), zs0 = su32(ZS);
-      int n1[2] = {0, 0}, n2[2] = {0, 0}, nF = 0;
-      long long last = clock64();
-      while (n2[0] < nt || (NQ == 2 && n2[1] < nt)) {
-        bool did = false;
+      // the Z buffer of each tile follows the key producers' rule: it flips
+      // whenever the tile's basis slot differs from the previous tile's
+      int cur_slot = -1, zb = 1, ab_read = 0;
+      int bs_next = nt > 0 ? a.tiles[t_begin].x : 0;
+      for (int t = 0; t < nt; ++t) {
+        if (__any_sync(0xffffffffu, ab_read != 0)) break;
+        const int bslot = bs_next;
+        if (t + 1 < nt) bs_next = a.tiles[t_begin + t + 1].x;
+        nbar_sync(kNbKc, KT + 32);
+        fence_after();
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
-          const int t = n1[g];
-          if (t < nt && n2[g] == t && warp_all(bar_test(kc_ready, (uint32_t)(t & 1)) &&
-                                               (t == 0 || bar_test(&pv_issued[g], (uint32_t)((t - 1) & 1))))) {
+          if (t > 0) {
+            nbar_sync(kNbPvi + g, 64);
             fence_after();
-            const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
-            if (elect_one()) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-                mma_ss(d, desc_sw128(qa + ko), desc_sw128(b1 + ko), kIdescS, j > 0);
-              }
-            }
-            __syncwarp();
-            ++n1[g];
-            did = true;
           }
-        }
-        if (nF < n1[0] && (NQ == 1 || nF < n1[1])) {
-          if (elect_one()) commit(b1_free);
+          const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
+          if (elect_one()) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+              mma_ss(d, desc_sw128(qa + ko), desc_sw128(b1 + ko), kIdescS, j > 0);
+            }
+          }
           __syncwarp();
-          ++nF;
+        }
+        if (elect_one()) commit(b1_free);
+        __syncwarp();
+        nbar_sync(kNbKr, KT + 32);
+        ab_read = abort_sh;   // after this tile's last wait; used before the next tile's first
+        fence_after();
+        if (RP > 0 && bslot != cur_slot) {
+          cur_slot = bslot;
+          zb ^= 1;
         }
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
-          const int t = n2[g];
-          if (t < n1[g] && warp_all(bar_test(kr_ready, (uint32_t)(t & 1)))) {
-            fence_after();
-            const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
-            const int z = RP > 0 ? ZSEL[0] : 0;
-            if (elect_one()) {
+          const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
+          if (elect_one()) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-                mma_ss(d, desc_sw128(qa + ko), desc_sw128(b2 + ko), kIdescS, 1);
-              }
-              if constexpr (RP > 0)
-                mma_ss(d, desc_none(zs0 + (z * 2 + g) * kZBuf, 128, 256), desc_none(es, 128, 256), kIdescS, 1);
-              commit(&s_done[g]);
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+              mma_ss(d, desc_sw128(qa + ko), desc_sw128(b2 + ko), kIdescS, 1);
             }
-            __syncwarp();
-            ++n2[g];
-            did = true;
+            if constexpr (RP > 0)
+              mma_ss(d, desc_none(zs0 + (zb * 2 + g) * kZBuf, 128, 256), desc_none(es, 128, 256), kIdescS, 1);
+            commit(&s_done[g]);
           }
-        }
-        if (did) {
-          last = clock64();
-        } else if (__any_sync(0xffffffffu, abort_sh != 0)) {
-          ok = false;
-          break;
-        } else if (__any_sync(0xffffffffu, clock64() - last > kWaitCycles)) {
-          if (lane == 0) {
-            abort_sh = 1;
-            atomicOr(a.status, kDevTimeout);
-          }
-          ok = false;
-          break;
+          __syncwarp();
         }
       }
     }
