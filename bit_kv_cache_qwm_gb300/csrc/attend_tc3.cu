@@ -29,9 +29,7 @@
 //                    tile: online softmax in the exp2 domain with a lazy
 //                    rescale of O (only when the running maximum grows by
 //                    more than 2^8), P in float16 over the first 64 columns
-//                    of S; once the tile's four warps have written P (a
-//                    128-thread named barrier) the first of them issues
-//                    O_g += P_g V_hat itself and signals the MMA warp.
+//                    of S, then arrive on the tile's "P written" barrier.
 //   warps 8-11       key producers, per tile: gather the centroid rows (B1,
 //                    asynchronous 16-byte copies) once the centroid parts of
 //                    the previous tile are done, then write the residuals
@@ -45,18 +43,17 @@
 //                    two groups run their loops independently, so the value
 //                    dequantisation of a tile overlaps the key work of the
 //                    next.
-//   warp 15          MMA issuer and TMEM owner: per tile, in a fixed order,
-//                    S_a = Q_a B1^T, S_b = Q_b B1^T (centroid parts), then
-//                    S_g += Q_g B2^T + Z_g E^T (residual and PSAC parts); the
-//                    whole warp waits, one elected lane issues (O_g += P_g
-//                    V_hat, A = P in TMEM, comes from the softmax warps of
-//                    tile g).  The centroid part of the next tile only needs
-//                    B1, so it runs on the tensor pipe while the producers
-//                    still compute B2.  S_g(t+1) is issued after PV_g(t), so
-//                    the tensor pipe's in-order execution keeps P_g(t) intact
-//                    until PV_g(t) has read it.
-// Handoffs between threads (V_hat written, B1 gathered, B2 written, PV issued)
-// use named barriers: an mbarrier wait goes through the shared-memory pipe,
+//   warp 15          MMA issuer and TMEM owner: per tile t, in a fixed order,
+//                    for g = a, b: O_g += P_g(t-1) V_hat(t-1) (A = P in
+//                    TMEM), S_g = Q_g B1^T (centroid part); then S_g +=
+//                    Q_g B2^T + Z_g E^T (residual and PSAC parts).  The whole
+//                    warp waits, one elected lane issues.  The centroid part
+//                    only needs B1, so it runs on the tensor pipe while the
+//                    producers still compute B2.  S_g(t) is issued after
+//                    PV_g(t-1), so the tensor pipe's in-order execution keeps
+//                    P_g(t-1) intact until PV_g(t-1) has read it.
+// Handoffs between threads (P written, V_hat written, B1 gathered, B2
+// written) use named barriers: an mbarrier wait goes through the shared-memory pipe,
 // which the MMAs' operand reads and the producers' stores keep busy (a wait
 // on a completed mbarrier then takes hundreds of cycles).  The tensor pipe's
 // completions (S done, PV done, B1 free) arrive on mbarriers.
@@ -134,28 +131,22 @@ struct Tc3Args {
 template <int KT>
 __device__ __forceinline__ void key_sync3() { asm volatile("bar.sync 1, %0;" ::"n"(KT) : "memory"); }
 __device__ __forceinline__ void val_sync3() { asm volatile("bar.sync 2, %0;" ::"n"(kValT) : "memory"); }
-// named barriers "V_hat of the tile written" for query tile g (5 + g): the
-// value producers arrive, the warp of tile g that issues PV_g waits.  A named
-// barrier does not pass through the shared-memory pipe, which the MMAs'
-// operand reads and the producers' stores keep busy, so the handoff costs
-// tens of cycles instead of hundreds.
-__device__ __forceinline__ void vready_arrive(int g) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(5 + g), "n"(kValT + 32) : "memory");
-}
-__device__ __forceinline__ void vready_sync(int g) {
-  asm volatile("bar.sync %0, %1;" ::"r"(5 + g), "n"(kValT + 32) : "memory");
-}
-// The MMA warp's inputs arrive on named barriers too: "PV_g issued" (7 + g;
-// the PV-issuing softmax warp of tile g arrives), "B1 gathered" (9) and "B2,
-// e, Z written" (10; the key producers arrive).  Whoever arrives does so once
+// named barrier "V_hat of the tile written" (5): the value producers arrive,
+// the MMA warp waits.  A named barrier does not pass through the
+// shared-memory pipe, which the MMAs' operand reads and the producers' stores
+// keep busy, so the handoff costs tens of cycles instead of hundreds.
+__device__ __forceinline__ void vready_arrive() { asm volatile("bar.arrive 5, %0;" ::"n"(kValT + 32) : "memory"); }
+__device__ __forceinline__ void vready_sync() { asm volatile("bar.sync 5, %0;" ::"n"(kValT + 32) : "memory"); }
+// The MMA warp's other inputs arrive on named barriers too: "P_g written" (7 +
+// g; the four softmax warps of tile g arrive), "B1 gathered" (9) and "B2, e,
+// Z written" (10; the key producers arrive).  Whoever arrives does so once
 // per tile, and once more for the tile it was on if it gives up; the MMA warp
 // reads the abort flag after each tile's last wait and stops at the next, so
 // no named-barrier wait is left without its arrival.
-constexpr int kNbPvi = 7, kNbKc = 9, kNbKr = 10;
+constexpr int kNbP = 7, kNbKc = 9, kNbKr = 10;
 __device__ __forceinline__ void nbar_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void nbar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 // named barriers of the softmax warps of query tile g (3 + g; 128 threads)
-__device__ __forceinline__ void soft_sync3(int g) { asm volatile("bar.sync %0, 128;" ::"r"(3 + g) : "memory"); }
 __device__ __forceinline__ bool soft_all3(int g, bool v) {
   uint32_t r;
   asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, %2, 128, p;\n"
@@ -357,8 +348,8 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       fence_async_smem();
       bar_arrive(q_ready);
     }
-    bool ok = true, pv_ab = false;
-    int ab_read = 0, t = 0;
+    bool ok = true;
+    int t = 0;
     for (; t < nt && ok; ++t) {
       const int nv = a.tiles[t_begin + t].y;
       if (!soft_all3(g, bar_wait(&s_done[g], (uint32_t)(t & 1), &abort_sh, a.status))) { ok = false; break; }
@@ -428,35 +419,13 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       tmem_wait_st();
       l_run += psum;
       fence_before();
-      // P_g(t) is complete once the tile's four warps are here; the first of
-      // them issues PV_g(t) itself (no handoff to the MMA warp), then lets
-      // the MMA warp order S_g(t+1) after it
-      soft_sync3(g);
-      if ((warp & 3) == 0) {
-        // V_hat(t) is written once the value producers have arrived (they
-        // arrive once more if they give up; once the abort flag, read after
-        // the previous wait, is set, this warp waits no more)
-        pv_ab = pv_ab || __any_sync(0xffffffffu, ab_read != 0);
-        if (!pv_ab) {
-          vready_sync(g);
-          ab_read = abort_sh;
-          fence_after();
-          if (elect_one()) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(su32(Vt) + 2048 * j), kIdescPV,
-                     (t > 0 || j > 0) ? 1u : 0u);
-            commit(&pv_done[g]);
-          }
-          __syncwarp();
-        }
-        fence_before();
-        if (t + 1 < nt) nbar_arrive(kNbPvi + g, 64);
-      }
+      // P_g(t) written: the MMA warp issues PV_g(t) once the tile's four
+      // warps have arrived
+      nbar_arrive(kNbP + g, 160);
     }
-    // a group that gave up before issuing PV_g(t) still lets the MMA warp pass
+    // a group that gave up before writing P_g(t) still lets the MMA warp pass
     // its wait for it
-    if (!ok && (warp & 3) == 0 && t + 1 < nt) nbar_arrive(kNbPvi + g, 64);
+    if (!ok && t < nt) nbar_arrive(kNbP + g, 160);
     if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
     fence_after();
     sm_ok = ok;
@@ -635,8 +604,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
         dq_block(Vt, key, b, w, qp);
       }
       fence_async_smem();
-      vready_arrive(0);
-      if (NQ == 2) vready_arrive(1);
+      vready_arrive();
       // refill ring stage t & 1 with tile t + 2 once both producer groups are done with it
       val_sync3();
       if (p == 0 && t + 2 < nt) {
@@ -648,47 +616,61 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     }
     // a group that gave up before arriving for its current tile arrives once
     // more, so that a softmax warp waiting for that tile's V_hat is released
-    if (!ok) {
-      vready_arrive(0);
-      if (NQ == 2) vready_arrive(1);
-    }
+    if (!ok) vready_arrive();
   } else {
     // ------------------------------------------------------------ MMA issuer
     bool ok = warp_all(bar_wait(q_ready, 0u, &abort_sh, a.status));
     fence_after();
-    // per tile, in a fixed order: the centroid parts S1_a(t), S1_b(t) (B1(t)
-    // gathered, PV_g(t-1) issued by the softmax warps of tile g), then the
-    // residual and PSAC parts S2_a(t), S2_b(t) (B2(t), e and Z written).  All
-    // waits are named barriers; the whole warp waits, one elected lane issues.
+    // per tile t, in a fixed order: for each query tile g, PV_g(t-1) (P_g(t-1)
+    // written by the softmax warps of tile g, V_hat(t-1) written) and then
+    // the centroid part S1_g(t) (B1(t) gathered), so that S_g(t) follows
+    // PV_g(t-1) in the tensor pipe and P_g(t-1), which lies over S_g, is read
+    // before it is overwritten; then the residual and PSAC parts S2_a(t),
+    // S2_b(t) (B2(t), e and Z written).  All waits are named barriers; the
+    // whole warp waits, one elected lane issues.
     if (ok) {
       const uint32_t qs0 = su32(Qs), b1 = su32(B1), b2 = su32(B2);
-      const uint32_t es = su32(Es), zs0 = su32(ZS);
+      const uint32_t es = su32(Es), zs0 = su32(ZS), vt = su32(Vt);
       // the Z buffer of each tile follows the key producers' rule: it flips
       // whenever the tile's basis slot differs from the previous tile's
       int cur_slot = -1, zb = 1, ab_read = 0;
       int bs_next = nt > 0 ? a.tiles[t_begin].x : 0;
-      for (int t = 0; t < nt; ++t) {
+      for (int t = 0; t <= nt; ++t) {
         if (__any_sync(0xffffffffu, ab_read != 0)) break;
         const int bslot = bs_next;
         if (t + 1 < nt) bs_next = a.tiles[t_begin + t + 1].x;
-        nbar_sync(kNbKc, KT + 32);
-        fence_after();
+        if (t < nt) {
+          nbar_sync(kNbKc, KT + 32);
+          fence_after();
+        }
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
           if (t > 0) {
-            nbar_sync(kNbPvi + g, 64);
+            nbar_sync(kNbP + g, 160);
+            if (g == 0) vready_sync();
             fence_after();
-          }
-          const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
-          if (elect_one()) {
+            if (elect_one()) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
-              mma_ss(d, desc_sw128(qa + ko), desc_sw128(b1 + ko), kIdescS, j > 0);
+              for (int j = 0; j < 8; ++j)
+                mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
+                       (t > 1 || j > 0) ? 1u : 0u);
+              commit(&pv_done[g]);
             }
+            __syncwarp();
           }
-          __syncwarp();
+          if (t < nt) {
+            const uint32_t d = tmem + 128u * g, qa = qs0 + kTileOp * g;
+            if (elect_one()) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const uint32_t ko = (j >> 2) * 16384 + (j & 3) * 32;
+                mma_ss(d, desc_sw128(qa + ko), desc_sw128(b1 + ko), kIdescS, j > 0);
+              }
+            }
+            __syncwarp();
+          }
         }
+        if (t == nt) break;
         if (elect_one()) commit(b1_free);
         __syncwarp();
         nbar_sync(kNbKr, KT + 32);
