@@ -352,7 +352,12 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     int t = 0;
     for (; t < nt && ok; ++t) {
       const int nv = a.tiles[t_begin + t].y;
-      if (!soft_all3(g, bar_wait(&s_done[g], (uint32_t)(t & 1), &abort_sh, a.status))) { ok = false; break; }
+      // one warp of the group polls the mbarrier (each poll is a trip through
+      // the busy shared-memory pipe); the vote hands the result to the others
+      if (!soft_all3(g, (warp & 3) != 0 || bar_wait(&s_done[g], (uint32_t)(t & 1), &abort_sh, a.status))) {
+        ok = false;
+        break;
+      }
       fence_after();
       const uint32_t sbase = tmem + lane_base + colS;
       // keys 64-127: their maximum; then keys 0-63, which stay in registers
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     sm_ok = ok;
   } else if (warp < kSoftW + kKeyW) {
     // ------------------------------------------------------------ key producers
-    const int p = tid - 128 * NQ;   // 0 .. KT - 1
+    const int p = tid - 128 * NQ, kw = p >> 5;   // 0 .. KT - 1, its warp in the group
     const uint32_t TB = (uint32_t)a.off.bytes;
     const __half* c16 = a.cent16 + (int64_t)h * a.nC * kD;
     int cur_slot = -1, zb = 1;
@@ -443,9 +448,16 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       kc_due = true;
       const uint8_t* tb = Ring + (t & 1) * TB;
       const uint32_t pp = (uint32_t)((t - 1) & 1);
-      if (!key_all3<KT>(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
+      // one warp of the group polls each mbarrier; the vote hands the result on
+      if (!key_all3<KT>(kw != 0 || bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) {
+        ok = false;
+        break;
+      }
       // ---- B1: the centroid parts of S_a(t-1) and S_b(t-1) have read it
-      if (t > 0 && !key_all3<KT>(bar_wait(b1_free, pp, &abort_sh, a.status))) { ok = false; break; }
+      if (t > 0 && !key_all3<KT>(kw != 0 || bar_wait(b1_free, pp, &abort_sh, a.status))) {
+        ok = false;
+        break;
+      }
       {
         // thread: one 16-byte chunk of NK consecutive keys, their indices in
         // one or two 16-byte loads (a warp covers whole 256-byte centroid rows)
@@ -484,8 +496,8 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       nbar_arrive(kNbKc, KT + 32);
       kc_due = false;
       // ---- B2, e, Z: S_a(t-1) and S_b(t-1) are complete
-      if (t > 0 && !key_all3<KT>(bar_wait(&s_done[0], pp, &abort_sh, a.status) &&
-                              (NQ == 1 || bar_wait(&s_done[1], pp, &abort_sh, a.status)))) {
+      if (t > 0 && !key_all3<KT>(kw != 0 || (bar_wait(&s_done[0], pp, &abort_sh, a.status) &&
+                                             (NQ == 1 || bar_wait(&s_done[1], pp, &abort_sh, a.status))))) {
         ok = false;
         break;
       }
@@ -576,7 +588,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     }
   } else if (warp < kMmaW) {
     // ------------------------------------------------------------ value producers
-    const int p = tid - (kSoftW + kKeyW) * 32;   // 0..95
+    const int p = tid - (kSoftW + kKeyW) * 32, vw = p >> 5;   // 0..95, its warp in the group
     const uint32_t TB = (uint32_t)a.off.bytes;
     const uint8_t* tiles_h = a.cache + (int64_t)h * a.max_tiles * a.off.bytes;
     bool ok = true;
@@ -589,10 +601,13 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     for (int t = 0; t < nt && ok; ++t) {
       const uint8_t* tb = Ring + (t & 1) * TB;
       const uint32_t pp = (uint32_t)((t - 1) & 1);
-      if (!val_all3(bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) { ok = false; break; }
+      if (!val_all3(vw != 0 || bar_wait(&full[t & 1], (uint32_t)((t >> 1) & 1), &abort_sh, a.status))) {
+        ok = false;
+        break;
+      }
       // ---- V_hat: PV_a(t-1) and PV_b(t-1) have read the previous one
-      if (t > 0 && !val_all3(bar_wait(&pv_done[0], pp, &abort_sh, a.status) &&
-                             (NQ == 1 || bar_wait(&pv_done[1], pp, &abort_sh, a.status)))) {
+      if (t > 0 && !val_all3(vw != 0 || (bar_wait(&pv_done[0], pp, &abort_sh, a.status) &&
+                                         (NQ == 1 || bar_wait(&pv_done[1], pp, &abort_sh, a.status))))) {
         ok = false;
         break;
       }
