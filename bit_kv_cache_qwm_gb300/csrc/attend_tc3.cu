@@ -137,13 +137,14 @@ __device__ __forceinline__ void val_sync3() { asm volatile("bar.sync 2, %0;" ::"
 // keep busy, so the handoff costs tens of cycles instead of hundreds.
 __device__ __forceinline__ void vready_arrive() { asm volatile("bar.arrive 5, %0;" ::"n"(kValT + 32) : "memory"); }
 __device__ __forceinline__ void vready_sync() { asm volatile("bar.sync 5, %0;" ::"n"(kValT + 32) : "memory"); }
-// The MMA warp's other inputs arrive on named barriers too: "P_g written" (7 +
-// g; the four softmax warps of tile g arrive), "B1 gathered" (9) and "B2, e,
-// Z written" (10; the key producers arrive).  Whoever arrives does so once
+// The MMA warp's other inputs arrive on named barriers too: "P_g of keys 0-63
+// written" (11 + g) and "P_g written" (7 + g; the four softmax warps of tile g
+// arrive), "B1 gathered" (9) and "B2, e, Z written" (10; the key producers
+// arrive).  Whoever arrives does so once
 // per tile, and once more for the tile it was on if it gives up; the MMA warp
 // reads the abort flag after each tile's last wait and stops at the next, so
 // no named-barrier wait is left without its arrival.
-constexpr int kNbP = 7, kNbKc = 9, kNbKr = 10;
+constexpr int kNbP = 7, kNbKc = 9, kNbKr = 10, kNbP1 = 11;
 __device__ __forceinline__ void nbar_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void nbar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 // named barriers of the softmax warps of query tile g (3 + g; 128 threads)
@@ -413,6 +414,10 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
       // 0-31, already read), then keys 64-127 again from TMEM (S columns
       // 64-127, untouched), whose P goes over columns 32-63
       float psum = nv >= 128 ? exp_keys<4, true>(v, 0, nv, c2v, mv, sbase) : exp_keys<4, false>(v, 0, nv, c2v, mv, sbase);
+      // P of keys 0-63 written: the MMA warp may start PV_g(t) on them
+      tmem_wait_st();
+      fence_before();
+      nbar_arrive(kNbP1 + g, 160);
 #pragma unroll 1
       for (int hq = 0; hq < 2; ++hq) {
         uint32_t w[32];
@@ -430,7 +435,10 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     }
     // a group that gave up before writing P_g(t) still lets the MMA warp pass
     // its wait for it
-    if (!ok && t < nt) nbar_arrive(kNbP + g, 160);
+    if (!ok && t < nt) {
+      nbar_arrive(kNbP1 + g, 160);
+      nbar_arrive(kNbP + g, 160);
+    }
     if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
     fence_after();
     sm_ok = ok;
@@ -658,17 +666,32 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
           nbar_sync(kNbKc, KT + 32);
           fence_after();
         }
+        if (t > 0) {
+          // the first half of PV_g(t-1) (keys 0-63) as soon as their P is
+          // written, while the softmax still works on keys 64-127
 #pragma unroll
-        for (int g = 0; g < NQ; ++g) {
-          if (t > 0) {
-            nbar_sync(kNbP + g, 160);
+          for (int g = 0; g < NQ; ++g) {
+            nbar_sync(kNbP1 + g, 160);
             if (g == 0) vready_sync();
             fence_after();
             if (elect_one()) {
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
+              for (int j = 0; j < 4; ++j)
                 mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV,
                        (t > 1 || j > 0) ? 1u : 0u);
+            }
+            __syncwarp();
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < NQ; ++g) {
+          if (t > 0) {
+            nbar_sync(kNbP + g, 160);
+            fence_after();
+            if (elect_one()) {
+#pragma unroll
+              for (int j = 4; j < 8; ++j)
+                mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV, 1u);
               commit(&pv_done[g]);
             }
             __syncwarp();
