@@ -138,13 +138,14 @@ __device__ __forceinline__ void val_sync3() { asm volatile("bar.sync 2, %0;" ::"
 __device__ __forceinline__ void vready_arrive() { asm volatile("bar.arrive 5, %0;" ::"n"(kValT + 32) : "memory"); }
 __device__ __forceinline__ void vready_sync() { asm volatile("bar.sync 5, %0;" ::"n"(kValT + 32) : "memory"); }
 // The MMA warp's other inputs arrive on named barriers too: "P_g of keys 0-63
-// written" (11 + g) and "P_g written" (7 + g; the four softmax warps of tile g
-// arrive), "B1 gathered" (9) and "B2, e, Z written" (10; the key producers
-// arrive).  Whoever arrives does so once
+// written" (11 + g), "P_g of keys 64-95 written" (13 + g) and "P_g written"
+// (7 + g; the four softmax warps of tile g arrive, and PV_g runs in three
+// parts as its keys' P is ready), "B1 gathered" (9) and "B2, e, Z written"
+// (10; the key producers arrive).  Whoever arrives does so once
 // per tile, and once more for the tile it was on if it gives up; the MMA warp
 // reads the abort flag after each tile's last wait and stops at the next, so
 // no named-barrier wait is left without its arrival.
-constexpr int kNbP = 7, kNbKc = 9, kNbKr = 10, kNbP1 = 11;
+constexpr int kNbP = 7, kNbKc = 9, kNbKr = 10, kNbP1 = 11, kNbP2 = 13;
 __device__ __forceinline__ void nbar_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void nbar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 // named barriers of the softmax warps of query tile g (3 + g; 128 threads)
@@ -425,6 +426,12 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
         tmem_wait_ld();
         psum += nv >= 128 ? exp_keys<2, true>(w, 64 + 32 * hq, nv, c2v, mv, sbase)
                           : exp_keys<2, false>(w, 64 + 32 * hq, nv, c2v, mv, sbase);
+        if (hq == 0) {
+          // P of keys 64-95 written too
+          tmem_wait_st();
+          fence_before();
+          nbar_arrive(kNbP2 + g, 160);
+        }
       }
       tmem_wait_st();
       l_run += psum;
@@ -437,6 +444,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
     // its wait for it
     if (!ok && t < nt) {
       nbar_arrive(kNbP1 + g, 160);
+      nbar_arrive(kNbP2 + g, 160);
       nbar_arrive(kNbP + g, 160);
     }
     if (ok && nt > 0) ok = warp_all(bar_wait(&pv_done[g], (uint32_t)((nt - 1) & 1), &abort_sh, a.status));
@@ -683,6 +691,20 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
             __syncwarp();
           }
         }
+        if (t > 0) {
+          // keys 64-95
+#pragma unroll
+          for (int g = 0; g < NQ; ++g) {
+            nbar_sync(kNbP2 + g, 160);
+            fence_after();
+            if (elect_one()) {
+#pragma unroll
+              for (int j = 4; j < 6; ++j)
+                mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV, 1u);
+            }
+            __syncwarp();
+          }
+        }
 #pragma unroll
         for (int g = 0; g < NQ; ++g) {
           if (t > 0) {
@@ -690,7 +712,7 @@ __global__ void __launch_bounds__(kThreads3, 1) attend_tc3_kernel(const Tc3Args 
             fence_after();
             if (elect_one()) {
 #pragma unroll
-              for (int j = 4; j < 8; ++j)
+              for (int j = 6; j < 8; ++j)
                 mma_ts(tmem + kColO + 128u * g, tmem + 128u * g + 8 * j, desc_sw128_mn(vt + 2048 * j), kIdescPV, 1u);
               commit(&pv_done[g]);
             }
