@@ -244,3 +244,22 @@ def test_attend_centroids_beyond_f16_fall_back(qwm):
     with pytest.raises(qwm.QwmError) as e:
         ctx.attend(_tensor(q, "bf16"))
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("kernel,m", [(1, 200), (2, 200), (3, 200), (4, 200), (6, 200), (6, 300), (5, 40), (7, 40)])
+def test_attend_basis_change_every_tile(qwm, kernel, m):
+    """A new basis version before every append of one tile or less (eight
+    versions, tails of 100, 1 and 128 slots): the PSAC term of every tile uses
+    another basis, so the tensor-core kernels switch their Z = q U_t^T buffer
+    on every tile."""
+    name = "bf16-h12-n32760"
+    sizes = [100, 128, 1, 77, 128, 64, 120, 128]
+    wl, ctx, cent, bases = _build(qwm, name, [0, 1], sizes, versions=len(sizes))
+    assert len(bases) == len(sizes)
+    ctx.set_attend_kernel(kernel)
+    q = synth.queries(wl, 2, [0, 1], m=m)
+    got = ctx.attend(_tensor(q, "bf16")).float().cpu().numpy()
+    assert ctx.status() == 0 and np.isfinite(got).all()
+    want, vmax = _oracle_on_gpu_bytes(ctx, cent, bases, q, [0, 1], 1 / np.sqrt(128))
+    err = np.abs(got - want).max()
+    assert err <= 1e-2 * vmax, (err, vmax)
