@@ -731,13 +731,18 @@ def run_small_m(args):
                      "frac": gbs / peaks["hbm_gbs"],
                      "traffic": profiled_traffic(os.path.join(ROOT, "profiles", f"attend_small_{wl.name}_m{M}.md"),
                                                  os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc", "attend_small.cu"))
-                     if kern == 5 else None,
+                     if kern == 5 else
+                     profiled_traffic(os.path.join(ROOT, "profiles", f"attend_tc3few_{wl.name}_m{M}.md"),
+                                      os.path.join(ROOT, "bit_kv_cache_qwm_gb300", "csrc", "attend_tc3.cu"))
+                     if kern == 7 else None,
                      "kernel": "qwm_attend",
                      "bytes_per_launch": nbytes, "peak_source": peaks["source"] + " HBM copy"},
         "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": q.numel() * q.element_size(),
                 "d2h_bytes_per_step": out.numel() * out.element_size(), "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * (3 if kern == 5 else 1),
+        # kernel 5: the QC table, the split attention and the merge; kernel 7:
+        # the split attention and the merge
+        "gpu_launches": args.steps * {5: 3, 7: 2}.get(kern, 1),
         "clocks": clk.summary(),
         "device_status": int(st),
         "attend_tflops": attend_flops(H, M, N, d, r) / (ms * 1e-3) / 1e12,
